@@ -1,0 +1,322 @@
+// Host side of the C ABI declared in include/kda.h: argument checks, the
+// workspace layout, TMA tensor maps, and the kernel launch sequence.
+// Nothing here allocates device memory or synchronises a stream, except
+// kda_get_device_status, whose job is to read the status word back.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "kda_internal.cuh"
+
+namespace kda {
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Tiled map over a token-major tensor [BT, H, D] viewed as (D, H, BT), boxes
+// of (box_d, 1, 64).
+bool map_tokens(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, int D, int H, long long BT,
+                int box_d, CUtensorMapSwizzle sw) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {cuuint64_t(D), cuuint64_t(H), cuuint64_t(BT)};
+  cuuint64_t strides[2] = {cuuint64_t(D) * esize, cuuint64_t(H) * D * esize};
+  cuuint32_t box[3] = {cuuint32_t(box_d), 1, 64};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, dt, 3, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Tiled map over a [rows, 64] bf16 matrix with SWIZZLE_128B boxes of (64, box_rows).
+bool map_rows64(CUtensorMap* m, const void* base, long long rows, int box_rows) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {64, cuuint64_t(rows)};
+  cuuint64_t strides[1] = {128};
+  cuuint32_t box[2] = {64, cuuint32_t(box_rows)};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct Layout {
+  size_t status = 0, nc = 4, idx = 0, off = 0, Qs = 0, Aqk_b = 0, KlT = 0, gamma = 0, W = 0, U = 0, total = 0;
+};
+
+struct Shape {
+  int B, T, Hq, Hv, K, V, N, varlen, NT, nc_max;
+  long long BT;
+};
+
+// Validates the sizes (not the pointers) and fills the derived counts.
+int check_shape(const KdaArgs* a, Shape* s) {
+  if (!a) return KDA_ERR_INVALID;
+  if (a->chunk <= 0) return KDA_ERR_INVALID;
+  if (a->chunk != kChunk) return KDA_ERR_UNSUPPORTED;
+  if (a->B < 1 || a->T < 0 || a->Hq < 1 || a->Hv < 1 || a->Hv % a->Hq != 0) return KDA_ERR_INVALID;
+  if ((a->K != 64 && a->K != 128) || (a->V != 64 && a->V != 128)) return KDA_ERR_UNSUPPORTED;
+  if (a->beta_dtype != KDA_DTYPE_BF16 && a->beta_dtype != KDA_DTYPE_FP32) return KDA_ERR_INVALID;
+  s->B = a->B;
+  s->T = a->T;
+  s->Hq = a->Hq;
+  s->Hv = a->Hv;
+  s->K = a->K;
+  s->V = a->V;
+  s->varlen = a->cu_seqlens != nullptr;
+  s->BT = (long long)a->B * a->T;
+  if (s->varlen) {
+    if (a->B != 1 || a->N < 0) return KDA_ERR_INVALID;
+    s->N = a->N;
+    s->NT = 0;
+    s->nc_max = s->N > 0 ? a->T / kChunk + s->N : 0;
+  } else {
+    s->N = a->B;
+    s->NT = (a->T + kChunk - 1) / kChunk;
+    s->nc_max = a->B * s->NT;
+  }
+  // 32-bit TMA coordinates and grid sizes
+  if (s->BT >= (1ll << 31) || (long long)s->nc_max * s->Hv * s->K >= (1ll << 31)) return KDA_ERR_UNSUPPORTED;
+  return KDA_OK;
+}
+
+Layout make_layout(const Shape& s, const KdaArgs* a, bool full) {
+  Layout L;
+  size_t p = kAlign;  // header: status word, chunk count
+  auto take = [&p](size_t bytes) {
+    const size_t at = p;
+    p = align_up(p + bytes);
+    return at;
+  };
+  if (s.varlen) {
+    L.idx = take(size_t(s.nc_max > 0 ? s.nc_max : 1) * 2 * 4);
+    L.off = take(size_t(s.N + 1) * 4);
+  }
+  if (full) {
+    L.Qs = take(size_t(s.BT) * s.Hv * s.K * 2);
+    L.Aqk_b = take(size_t(s.BT) * s.Hv * 64 * 2);
+    L.KlT = take(size_t(s.nc_max) * s.Hv * s.K * 64 * 2);
+    L.gamma = take(size_t(s.nc_max) * s.Hv * s.K * 4);
+    if (!a->W) L.W = take(size_t(s.BT) * s.Hv * s.K * 2);
+    if (!a->U) L.U = take(size_t(s.BT) * s.Hv * s.V * 2);
+  }
+  L.total = p;
+  return L;
+}
+
+int check_arch() {
+  int dev = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KDA_ERR_ARCH;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return KDA_ERR_ARCH;
+  if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return KDA_ERR_ARCH;
+  return (major == 10 && minor == 3) ? KDA_OK : KDA_ERR_ARCH;
+}
+
+int check_inputs(const KdaArgs* a, const void* ws) {
+  if (!a->q || !a->k || !a->v || !a->g || !a->beta) return KDA_ERR_INVALID;
+  const void* ptrs[] = {a->q, a->k, a->v, a->g, a->beta, a->cu_seqlens, a->initial_state, a->o,
+                        a->final_state, a->Aqk, a->Akk_inv, a->W, a->U, a->G};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return KDA_ERR_MISALIGNED;
+  if (ws && (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1))) return KDA_ERR_MISALIGNED;
+  return KDA_OK;
+}
+
+Problem make_problem(const Shape& s, const KdaArgs* a, uint8_t* ws, const Layout& L) {
+  Problem P{};
+  P.B = s.B;
+  P.T = s.T;
+  P.Hq = s.Hq;
+  P.Hv = s.Hv;
+  P.K = s.K;
+  P.V = s.V;
+  P.N = s.N;
+  P.NT = s.NT;
+  P.nc_max = s.nc_max;
+  P.varlen = s.varlen;
+  P.beta_fp32 = a->beta_dtype == KDA_DTYPE_FP32;
+  P.scale = a->scale;
+  P.cu = a->cu_seqlens;
+  P.status = reinterpret_cast<int32_t*>(ws + L.status);
+  if (s.varlen) {
+    P.chunk_idx = reinterpret_cast<const int32_t*>(ws + L.idx);
+    P.chunk_off = reinterpret_cast<const int32_t*>(ws + L.off);
+    P.nc_dev = reinterpret_cast<const int32_t*>(ws + L.nc);
+  }
+  return P;
+}
+
+// Shared front half of both entry points: checks, status reset, chunk table.
+int prologue(const KdaArgs* a, void* workspace, size_t ws_bytes, cudaStream_t st, bool full, Shape* s,
+             Layout* L) {
+  int rc = check_shape(a, s);
+  if (rc) return rc;
+  if (!workspace) return KDA_ERR_INVALID;
+  rc = check_inputs(a, workspace);
+  if (rc) return rc;
+  *L = make_layout(*s, a, full);
+  if (ws_bytes < L->total) return KDA_ERR_WORKSPACE;
+  rc = check_arch();
+  if (rc) return rc;
+  if (!encode_fn()) return KDA_ERR_LAUNCH;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  if (cudaMemsetAsync(ws, 0, 8, st) != cudaSuccess) return KDA_ERR_LAUNCH;
+  if (s->varlen && s->N > 0) {
+    if (launch_chunk_index(a->cu_seqlens, s->N, s->T, kChunk, reinterpret_cast<int32_t*>(ws + L->idx),
+                           reinterpret_cast<int32_t*>(ws + L->off), reinterpret_cast<int32_t*>(ws + L->nc),
+                           reinterpret_cast<int32_t*>(ws + L->status), st) != cudaSuccess)
+      return KDA_ERR_LAUNCH;
+  }
+  return KDA_OK;
+}
+
+int run_intra(const Shape& s, const KdaArgs* a, const Problem& P, const IntraOut& out, cudaStream_t st) {
+  IntraMaps m;
+  const auto bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const auto none = CU_TENSOR_MAP_SWIZZLE_NONE;
+  if (!map_tokens(&m.q, a->q, bf, 2, s.K, s.Hq, s.BT, s.K, none) ||
+      !map_tokens(&m.k, a->k, bf, 2, s.K, s.Hq, s.BT, s.K, none) ||
+      !map_tokens(&m.v, a->v, bf, 2, s.V, s.Hv, s.BT, s.V, none) ||
+      !map_tokens(&m.g, a->g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, s.K, s.Hv, s.BT, s.K, none))
+    return KDA_ERR_LAUNCH;
+  return launch_intra(P, m, a->beta, out, st) == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
+}
+
+}  // namespace
+}  // namespace kda
+
+using namespace kda;
+
+extern "C" size_t kda_workspace_size(const KdaArgs* a) {
+  Shape s;
+  if (check_shape(a, &s) != KDA_OK) return 0;
+  return make_layout(s, a, true).total;
+}
+
+extern "C" int kda_chunk_fwd(const KdaArgs* a, void* workspace, size_t ws_bytes, kda_stream_t stream) {
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  Shape s;
+  Layout L;
+  if (a && !a->o) return KDA_ERR_INVALID;
+  int rc = prologue(a, workspace, ws_bytes, st, true, &s, &L);
+  if (rc) return rc;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cudaEvent_t const* ev = reinterpret_cast<cudaEvent_t const*>(a->profile_events);
+  if (ev && cudaEventRecord(ev[0], st) != cudaSuccess) return KDA_ERR_LAUNCH;
+  if (s.BT == 0 || s.nc_max == 0) {
+    // no tokens: the final state is the initial state
+    if (a->final_state) {
+      const size_t bytes = size_t(s.N) * s.Hv * s.K * s.V * 4;
+      cudaError_t e = a->initial_state
+                          ? cudaMemcpyAsync(a->final_state, a->initial_state, bytes, cudaMemcpyDeviceToDevice, st)
+                          : cudaMemsetAsync(a->final_state, 0, bytes, st);
+      if (e != cudaSuccess) return KDA_ERR_LAUNCH;
+    }
+    return KDA_OK;
+  }
+  const Problem P = make_problem(s, a, ws, L);
+  IntraOut out{};
+  out.Aqk = a->Aqk;
+  out.Akk_inv = a->Akk_inv;
+  out.W = a->W ? a->W : ws + L.W;
+  out.U = a->U ? a->U : ws + L.U;
+  out.G = a->G;
+  out.Qs = ws + L.Qs;
+  out.Aqk_b = ws + L.Aqk_b;
+  out.KlT = ws + L.KlT;
+  out.gamma = reinterpret_cast<float*>(ws + L.gamma);
+  rc = run_intra(s, a, P, out, st);
+  if (rc) return rc;
+  if (ev && cudaEventRecord(ev[1], st) != cudaSuccess) return KDA_ERR_LAUNCH;
+
+  StateMaps m;
+  const auto bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
+  if (!map_tokens(&m.W, out.W, bf, 2, s.K, s.Hv, s.BT, 64, sw) ||
+      !map_tokens(&m.Qs, out.Qs, bf, 2, s.K, s.Hv, s.BT, 64, sw) ||
+      !map_tokens(&m.Aqk_b, out.Aqk_b, bf, 2, 64, s.Hv, s.BT, 64, sw) ||
+      !map_tokens(&m.U, out.U, bf, 2, s.V, s.Hv, s.BT, s.V, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !map_rows64(&m.KlT, out.KlT, (long long)s.nc_max * s.Hv * s.K, s.K))
+    return KDA_ERR_LAUNCH;
+  if (launch_state(P, m, out.gamma, a->initial_state, a->o, a->final_state, st) != cudaSuccess)
+    return KDA_ERR_LAUNCH;
+  if (ev && cudaEventRecord(ev[2], st) != cudaSuccess) return KDA_ERR_LAUNCH;
+  return KDA_OK;
+}
+
+extern "C" int kda_fwd_intra(const KdaArgs* a, void* workspace, size_t ws_bytes, kda_stream_t stream) {
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  Shape s;
+  Layout L;
+  if (a && (!a->Aqk || !a->Akk_inv || !a->W || !a->U)) return KDA_ERR_INVALID;
+  int rc = prologue(a, workspace, ws_bytes, st, false, &s, &L);
+  if (rc) return rc;
+  if (s.BT == 0 || s.nc_max == 0) return KDA_OK;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const Problem P = make_problem(s, a, ws, L);
+  IntraOut out{};
+  out.Aqk = a->Aqk;
+  out.Akk_inv = a->Akk_inv;
+  out.W = a->W;
+  out.U = a->U;
+  out.G = a->G;
+  return run_intra(s, a, P, out, st);
+}
+
+extern "C" int kda_prepare_chunk_indices(const int32_t* cu_seqlens, int32_t N, int32_t T, int32_t chunk,
+                                         int32_t* chunk_indices, int32_t* chunk_offsets, int32_t* num_chunks,
+                                         int32_t* status, kda_stream_t stream) {
+  if (chunk <= 0 || N < 0 || T < 0) return KDA_ERR_INVALID;
+  if (!cu_seqlens || !chunk_offsets || !num_chunks || !status || (N > 0 && !chunk_indices))
+    return KDA_ERR_INVALID;
+  const int rc = check_arch();
+  if (rc) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  return launch_chunk_index(cu_seqlens, N, T, chunk, chunk_indices, chunk_offsets, num_chunks, status, st) ==
+                 cudaSuccess
+             ? KDA_OK
+             : KDA_ERR_LAUNCH;
+}
+
+extern "C" int kda_get_device_status(const void* workspace, kda_stream_t stream, int32_t* status_out) {
+  if (!workspace || !status_out) return KDA_ERR_INVALID;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, workspace, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess) return KDA_ERR_LAUNCH;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return KDA_ERR_LAUNCH;
+  *status_out = v;
+  return KDA_OK;
+}
+
+extern "C" const char* kda_status_string(int status) {
+  switch (status) {
+    case KDA_OK: return "ok";
+    case KDA_ERR_INVALID: return "invalid argument";
+    case KDA_ERR_UNSUPPORTED: return "unsupported size (chunk must be 64; K, V in {64, 128})";
+    case KDA_ERR_MISALIGNED: return "misaligned pointer (16 B for tensors, 256 B for the workspace)";
+    case KDA_ERR_ARCH: return "device is not sm_103 (the library is built for sm_103a)";
+    case KDA_ERR_LAUNCH: return "CUDA launch or tensor-map encode failed";
+    case KDA_ERR_WORKSPACE: return "workspace smaller than kda_workspace_size()";
+    case KDA_ERR_BAD_SEQLENS: return "cu_seqlens must start at 0, be non-decreasing and end at T";
+    case KDA_ERR_TIMEOUT: return "a bounded wait inside a kernel ran out";
+    default: return "unknown status";
+  }
+}

@@ -1,0 +1,115 @@
+// Internal declarations shared by the host API and the kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/kda.h"
+#include "kda_ptx.cuh"
+
+namespace kda {
+
+constexpr int kChunk = 64;                          // rows per chunk
+constexpr uint64_t kWaitLimitNs = 2000000000ull;    // bounded waits: 2 s
+
+// Sizes and chunk bookkeeping of one call, passed by value to every kernel.
+struct Problem {
+  int B, T, Hq, Hv, K, V;
+  int N;             // sequences (B for fixed length)
+  int NT;            // fixed length: chunks per sequence (ceil(T / 64)); varlen: 0
+  int nc_max;        // upper bound on the chunk count (grid size)
+  int varlen;        // 1 when cu_seqlens is given
+  int beta_fp32;     // 1: beta is fp32, 0: bf16
+  float scale;
+  const int32_t* cu;         // varlen: cu_seqlens
+  const int32_t* chunk_idx;  // varlen: [nc, 2] (sequence, chunk within sequence)
+  const int32_t* chunk_off;  // varlen: [N + 1]
+  const int32_t* nc_dev;     // varlen: number of chunks
+  int32_t* status;           // device status word
+};
+
+// One chunk: flat token row t0 (into the [B*T] token axis), L valid rows,
+// its sequence n and index i within that sequence.
+struct ChunkInfo {
+  int n, i, t0, L;
+  bool valid;
+};
+
+__device__ __forceinline__ ChunkInfo chunk_info(const Problem& P, int gc) {
+  ChunkInfo c{0, 0, 0, 0, false};
+  int bos, len;
+  if (!P.varlen) {
+    c.n = gc / P.NT;
+    c.i = gc - c.n * P.NT;
+    bos = c.n * P.T;
+    len = P.T;
+  } else {
+    if (gc >= *P.nc_dev) return c;
+    c.n = P.chunk_idx[2 * gc];
+    c.i = P.chunk_idx[2 * gc + 1];
+    bos = P.cu[c.n];
+    len = P.cu[c.n + 1] - bos;
+  }
+  c.t0 = bos + c.i * kChunk;
+  c.L = min(kChunk, len - c.i * kChunk);
+  c.valid = c.L > 0;
+  return c;
+}
+
+// Record the first device error (later ones are dropped).
+__device__ __forceinline__ void set_status(int32_t* status, int32_t code) {
+  atomicCAS(reinterpret_cast<int*>(status), 0, code);
+}
+
+// Bounded mbarrier wait shared by all threads of a CTA.  After kWaitLimitNs it
+// records KDA_ERR_TIMEOUT, raises the CTA's abort flag (later waits return at
+// once) and returns false; the caller carries on to its normal exit.
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                         int32_t* status) {
+  if (*abort_flag) return false;
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      set_status(status, KDA_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// ---- host-side launchers (defined next to their kernels) ----
+struct IntraOut {
+  float* Aqk;       // fp32 [BT, Hv, 64] (may be null)
+  float* Akk_inv;   // fp32 [BT, Hv, 64] (may be null)
+  void* W;          // bf16 [BT, Hv, K]  (required)
+  void* U;          // bf16 [BT, Hv, V]  (required)
+  float* G;         // fp32 [BT, Hv, K]  (may be null)
+  // state-pass operands (null in the standalone intra primitive)
+  void* Qs;         // bf16 [BT, Hv, K]: scale * q * e^G
+  void* Aqk_b;      // bf16 [BT, Hv, 64]: Aqk rounded for the output MMA
+  void* KlT;        // bf16 [nc_max, Hv, K, 64]: (k * e^{G_last - G})^T per chunk
+  float* gamma;     // fp32 [nc_max, Hv, K]: e^{G_last}
+};
+
+struct IntraMaps {
+  CUtensorMap q, k, v, g;
+};
+
+struct StateMaps {
+  CUtensorMap W, Qs, Aqk_b, U, KlT;
+};
+
+cudaError_t launch_chunk_index(const int32_t* cu, int N, int T, int chunk, int32_t* idx, int32_t* off,
+                               int32_t* nc, int32_t* status, cudaStream_t s);
+cudaError_t launch_intra(const Problem& P, const IntraMaps& maps, const void* beta, const IntraOut& out,
+                         cudaStream_t s);
+cudaError_t launch_state(const Problem& P, const StateMaps& maps, const float* gamma, const float* h0,
+                         void* o, float* hT, cudaStream_t s);
+
+}  // namespace kda

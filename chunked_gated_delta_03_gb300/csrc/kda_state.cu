@@ -1,0 +1,274 @@
+// Inter-chunk state pass and output: one CTA per (sequence, value head),
+// sequential over the sequence's chunks, with the K x V state on chip.
+// This is the delta-H state kernel plus the output kernel of cuLA
+// REPO_LAYOUT.md (ops/chunk_delta_h.py, ops/fwd_o.py), fused.
+//
+// Everything is computed transposed so that every MMA has M = 128 (the value
+// channel v, one TMEM lane per v) and all operands are K-major SWIZZLE_128B:
+//   P^T  = S^T W^T                  (M=128 v, N=64 rows, K=K)     TMEM cols   0..63
+//   O^T  = S^T Qs^T + Delta^T Aqk^T (M=128 v, N=64 rows, K=K, 64) TMEM cols  64..191 (2 buffers)
+//   H^T  = Delta^T Kl               (M=128 v, N=K,       K=64)    TMEM cols 192..
+// with Delta = U - W S (rows past the chunk's L valid rows forced to 0),
+// Qs = scale q e^G, Kl = k e^{G_last - G}, and the update
+//   S <- Diag(e^{G_last}) S + Kl^T Delta.
+// Epilogue thread v keeps column v of S (K fp32 values) in registers and
+// writes its bf16 copy as row v of the A operand S^T for the next chunk.
+//
+// Warp roles: warp 0 issues TMA loads into a 2-stage ring, warp 1 issues the
+// MMAs, warps 2-5 (128 threads) run the epilogue.
+#include "kda_internal.cuh"
+
+namespace kda {
+
+namespace {
+
+constexpr int kStateThreads = 192;
+constexpr int kStages = 2;
+
+template <int K, int V>
+struct StateLayout {
+  // one pipeline stage
+  static constexpr uint32_t W = 0;                        // 64 x K, K-major SW128
+  static constexpr uint32_t Qs = W + 64 * K * 2;          // 64 x K
+  static constexpr uint32_t Aqk = Qs + 64 * K * 2;        // 64 x 64
+  static constexpr uint32_t Kl = Aqk + 64 * 64 * 2;       // K x 64 (Kl^T rows = k)
+  static constexpr uint32_t U = Kl + K * 64 * 2;          // 64 x V, plain row-major
+  static constexpr uint32_t gam = U + 64 * V * 2;         // K floats
+  static constexpr uint32_t stage_bytes = ((gam + K * 4) + 1023) / 1024 * 1024;
+  static constexpr uint32_t S = kStages * stage_bytes;    // 128 x K, K-major SW128 (A operand S^T)
+  static constexpr uint32_t D = S + 128 * K * 2;          // 128 x 64 (A operand Delta^T)
+  static constexpr uint32_t bars = D + 128 * 64 * 2;      // full[2], empty[2], P, H, sready, dready
+  static constexpr uint32_t tmem_slot = bars + 8 * 8;
+  static constexpr uint32_t abort_slot = tmem_slot + 4;
+  static constexpr uint32_t total = abort_slot + 4;
+  static constexpr uint32_t bytes = total + 1024;
+  static constexpr uint32_t tx_bytes = 64 * K * 2 * 2 + 64 * 64 * 2 + K * 64 * 2 + 64 * V * 2 + K * 4;
+  static_assert(bytes <= 227 * 1024, "shared memory budget");
+};
+
+template <int K>
+__device__ __forceinline__ void store_state_row(uint8_t* sS, int v, const float (&S)[K]) {
+#pragma unroll
+  for (int c = 0; c < K; c += 8) {
+    const uint4 pk = make_uint4(pack_bf16x2(S[c], S[c + 1]), pack_bf16x2(S[c + 2], S[c + 3]),
+                                pack_bf16x2(S[c + 4], S[c + 5]), pack_bf16x2(S[c + 6], S[c + 7]));
+    *reinterpret_cast<uint4*>(sS + sw128_offset(v, c, 128)) = pk;
+  }
+}
+
+template <int K, int V>
+__global__ void __launch_bounds__(kStateThreads, 1)
+    state_kernel(const Problem P, const __grid_constant__ StateMaps maps, const float* __restrict__ gamma,
+                 const float* __restrict__ h0, __nv_bfloat16* __restrict__ o, float* __restrict__ hT) {
+  using Lay = StateLayout<K, V>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+  const int hv = blockIdx.x % P.Hv;
+  const int n = blockIdx.x / P.Hv;
+  if (*reinterpret_cast<volatile int32_t*>(P.status) != 0) return;
+  int bos, len, gc0;
+  if (P.varlen) {
+    bos = P.cu[n];
+    len = P.cu[n + 1] - bos;
+    gc0 = P.chunk_off[n];
+  } else {
+    bos = n * P.T;
+    len = P.T;
+    gc0 = n * P.NT;
+  }
+  const int nch = (len + kChunk - 1) / kChunk;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + Lay::bars);
+  uint64_t* empty = full + 2;
+  uint64_t* bar_P = full + 4;
+  uint64_t* bar_H = full + 5;
+  uint64_t* sready = full + 6;
+  uint64_t* dready = full + 7;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + Lay::tmem_slot);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + Lay::abort_slot);
+
+  if (tid == 0) {
+    *abort_flag = 0;
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1 + 4);
+    }
+    mbar_init(bar_P, 1);
+    mbar_init(bar_H, 1);
+    mbar_init(sready, 128);
+    mbar_init(dready, 128);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      for (int c = 0; c < nch; ++c) {
+        const int s = c & 1;
+        if (c >= kStages) wait_bar(&empty[s], ((c >> 1) - 1) & 1, abort_flag, P.status);
+        uint8_t* st = sm + s * Lay::stage_bytes;
+        const int t0 = bos + c * kChunk;
+        const int gc = gc0 + c;
+        mbar_arrive_expect_tx(&full[s], Lay::tx_bytes);
+#pragma unroll
+        for (int a = 0; a < K / 64; ++a) {
+          tma_load_3d(st + Lay::W + a * 64 * 128, &maps.W, a * 64, hv, t0, &full[s]);
+          tma_load_3d(st + Lay::Qs + a * 64 * 128, &maps.Qs, a * 64, hv, t0, &full[s]);
+        }
+        tma_load_3d(st + Lay::Aqk, &maps.Aqk_b, 0, hv, t0, &full[s]);
+        tma_load_2d(st + Lay::Kl, &maps.KlT, 0, (gc * P.Hv + hv) * K, &full[s]);
+        tma_load_3d(st + Lay::U, &maps.U, 0, hv, t0, &full[s]);
+        bulk_load(st + Lay::gam, gamma + (size_t(gc) * P.Hv + hv) * K, K * 4, &full[s]);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id64 = idesc_bf16_f32(128, 64);
+      constexpr uint32_t idK = idesc_bf16_f32(128, K);
+      const uint32_t sS = smem_u32(sm + Lay::S), sD = smem_u32(sm + Lay::D);
+      for (int c = 0; c < nch; ++c) {
+        const int s = c & 1;
+        const uint32_t st = smem_u32(sm + s * Lay::stage_bytes);
+        const uint32_t ocol = 64 + 64 * (c & 1);
+        wait_bar(&full[s], (c >> 1) & 1, abort_flag, P.status);
+        wait_bar(sready, c & 1, abort_flag, P.status);
+        tc_fence_after();
+        umma_kloop(tmem + 0, sS, 128, st + Lay::W, 64, K / 16, id64, 0);
+        umma_kloop(tmem + ocol, sS, 128, st + Lay::Qs, 64, K / 16, id64, 0);
+        umma_commit(bar_P);
+        wait_bar(dready, c & 1, abort_flag, P.status);
+        tc_fence_after();
+        umma_kloop(tmem + ocol, sD, 128, st + Lay::Aqk, 64, 4, id64, 1);
+        umma_kloop(tmem + 192, sD, 128, st + Lay::Kl, K, 4, idK, 0);
+        umma_commit(bar_H);
+        umma_commit(&empty[s]);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q4 = warp & 3;           // TMEM lane quadrant of this warp
+    const int v = 32 * q4 + lane;      // value channel owned by this thread
+    const bool vv = v < V;
+    uint8_t* sS = sm + Lay::S;
+    uint8_t* sD = sm + Lay::D;
+    float S[K];
+    const size_t hbase = (size_t(n) * P.Hv + hv) * K;
+#pragma unroll
+    for (int k = 0; k < K; ++k) S[k] = (h0 && vv) ? h0[(hbase + k) * V + v] : 0.f;
+    store_state_row<K>(sS, v, S);
+    fence_proxy_async_smem();
+    mbar_arrive(sready);
+    for (int c = 0; c < nch; ++c) {
+      const int s = c & 1;
+      const uint8_t* st = sm + s * Lay::stage_bytes;
+      const int t0 = bos + c * kChunk;
+      const int L = min(kChunk, len - c * kChunk);
+      const uint32_t ocol = 64 + 64 * (c & 1);
+      // Delta^T row v = U[:, v] - P^T row v, rows >= L zeroed
+      wait_bar(bar_P, c & 1, abort_flag, P.status);
+      wait_bar(&full[s], (c >> 1) & 1, abort_flag, P.status);
+      tc_fence_after();
+      const __nv_bfloat16* sU = reinterpret_cast<const __nv_bfloat16*>(st + Lay::U);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pr[32];
+        tmem_ld_x32(tmem_addr(tmem, 32 * q4, 32 * half), pr);
+#pragma unroll
+        for (int j = 0; j < 32; j += 8) {
+          float d[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int i = 32 * half + j + e;
+            const float u = vv ? __bfloat162float(sU[i * V + v]) : 0.f;
+            d[e] = (i < L) ? u - __uint_as_float(pr[j + e]) : 0.f;
+          }
+          const uint4 pk = make_uint4(pack_bf16x2(d[0], d[1]), pack_bf16x2(d[2], d[3]),
+                                      pack_bf16x2(d[4], d[5]), pack_bf16x2(d[6], d[7]));
+          *reinterpret_cast<uint4*>(sD + sw128_offset(v, 32 * half + j, 128)) = pk;
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(dready);
+      // state update S <- gamma * S + H
+      wait_bar(bar_H, c & 1, abort_flag, P.status);
+      tc_fence_after();
+      const float* sg = reinterpret_cast<const float*>(st + Lay::gam);
+#pragma unroll
+      for (int kb = 0; kb < K / 32; ++kb) {
+        uint32_t hr[32];
+        tmem_ld_x32(tmem_addr(tmem, 32 * q4, 192 + 32 * kb), hr);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) S[32 * kb + j] = fmaf(sg[32 * kb + j], S[32 * kb + j], __uint_as_float(hr[j]));
+      }
+      store_state_row<K>(sS, v, S);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(sready);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+      // O of this chunk sits in its own TMEM buffer; the next chunk writes the
+      // other one, and the chunk after that waits for this thread's next
+      // sready arrival, which comes after these loads.
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t orow[32];
+        tmem_ld_x32(tmem_addr(tmem, 32 * q4, ocol + 32 * half), orow);
+        if (vv) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int r = 32 * half + j;
+            if (r < L) o[(size_t(t0 + r) * P.Hv + hv) * V + v] = __float2bfloat16_rn(__uint_as_float(orow[j]));
+          }
+        }
+      }
+    }
+    if (hT && vv) {
+#pragma unroll
+      for (int k = 0; k < K; ++k) hT[(hbase + k) * V + v] = S[k];
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int K, int V>
+cudaError_t launch_state_t(const Problem& P, const StateMaps& maps, const float* gamma, const float* h0, void* o,
+                           float* hT, cudaStream_t s) {
+  constexpr uint32_t smem = StateLayout<K, V>::bytes;
+  cudaError_t e = cudaFuncSetAttribute(state_kernel<K, V>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const long long grid = (long long)P.N * P.Hv;
+  if (grid <= 0) return cudaSuccess;
+  state_kernel<K, V><<<unsigned(grid), kStateThreads, smem, s>>>(P, maps, gamma, h0,
+                                                                  reinterpret_cast<__nv_bfloat16*>(o), hT);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_state(const Problem& P, const StateMaps& maps, const float* gamma, const float* h0, void* o,
+                         float* hT, cudaStream_t s) {
+  if (P.K == 128 && P.V == 128) return launch_state_t<128, 128>(P, maps, gamma, h0, o, hT, s);
+  if (P.K == 128 && P.V == 64) return launch_state_t<128, 64>(P, maps, gamma, h0, o, hT, s);
+  if (P.K == 64 && P.V == 128) return launch_state_t<64, 128>(P, maps, gamma, h0, o, hT, s);
+  if (P.K == 64 && P.V == 64) return launch_state_t<64, 64>(P, maps, gamma, h0, o, hT, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace kda

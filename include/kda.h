@@ -1,0 +1,158 @@
+/*
+ * kda.h -- C ABI of the GB300 (sm_103a) chunked KDA forward library (libkda.so).
+ *
+ * KDA (Kimi Delta Attention) is the delta rule with a per-channel forget gate.
+ * Per value head, with state S in R^{K x V}, each token t applies
+ *     S_t = (I - beta_t k_t k_t^T) Diag(exp(g_t)) S_{t-1} + beta_t k_t v_t^T
+ *     o_t = scale * S_t^T q_t
+ * The library computes it chunk by chunk (chunk = 64 tokens), in the modular
+ * order of cuLA REPO_LAYOUT.md (cula/kda/chunk_fwd.py, chunk_intra.py, then
+ * ops/chunk_delta_h.py and ops/fwd_o.py) and of cuLA PR #131 (Summary: the
+ * intra-chunk matrices, the FP32 inverse of (I + Akk), the W/U recompute):
+ *   1. in-chunk inclusive cumsum of the log-gates, G;
+ *   2. Aqk[r,i] = scale sum_c q_r[c] k_i[c] e^{G_r[c]-G_i[c]} (i <= r) and
+ *      Akk[r,i] = beta_r sum_c k_r[c] k_i[c] e^{G_r[c]-G_i[c]} (i < r);
+ *   3. Akk_inv = (I + Akk)^{-1} in FP32;
+ *   4. W = Akk_inv (beta * k * e^G), U = Akk_inv (beta * v);
+ *   5. per chunk in order: Delta = U - W S, O = scale (q * e^G) S + Aqk Delta,
+ *      S <- Diag(e^{G_last}) S + (k * e^{G_last - G})^T Delta.
+ *
+ * Conventions for every entry point
+ *   - Pointers marked (device) are CUDA device pointers on the current device;
+ *     all tensors are dense, contiguous and token-major:
+ *       q, k      bf16 [B, T, Hq, K]
+ *       v         bf16 [B, T, Hv, V]
+ *       g         fp32 [B, T, Hv, K]   (log-gates, already activated)
+ *       beta      bf16 or fp32 [B, T, Hv]
+ *       o         bf16 [B, T, Hv, V]
+ *       Aqk, Akk_inv  fp32 [B, T, Hv, 64]  (row t holds row t - t0 of its
+ *                     chunk's 64 x 64 matrix; columns past the chunk's valid
+ *                     rows are zero)
+ *       W         bf16 [B, T, Hv, K];  U bf16 [B, T, Hv, V]
+ *       G         fp32 [B, T, Hv, K]   (in-chunk cumsum of g)
+ *       initial_state / final_state  fp32 [N, Hv, K, V], N = B (fixed length)
+ *                     or the number of packed sequences (varlen)
+ *   - Packed varlen (cuLA PR #131, Summary): pass cu_seqlens (int32 [N+1],
+ *     cu[0] = 0, non-decreasing, cu[N] = T) and B = 1.
+ *   - Grouped-value heads: Hv % Hq == 0; value head hv reads q/k head hv / (Hv / Hq).
+ *   - Supported sizes: chunk == 64; K, V in {64, 128}; T >= 0; Hq, Hv >= 1.
+ *   - Every base address must be 16-byte aligned (TMA); the workspace 256-byte.
+ *   - Ownership: the caller owns every buffer, outputs and workspace included.
+ *     The library allocates no device memory, keeps no state between calls,
+ *     and performs no host<->device synchronisation; all work is enqueued on
+ *     `stream` in order.  Calls on different streams with different
+ *     workspaces are independent.
+ *   - Errors: host-side argument checks return a negative kda_status before
+ *     anything is enqueued.  Errors found on the device (bad cu_seqlens, a
+ *     bounded wait that ran out) are written to the status word at the start
+ *     of the workspace; read it with kda_get_device_status.  No entry point
+ *     throws, aborts or traps.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* kda_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+enum kda_status {
+  KDA_OK = 0,
+  KDA_ERR_INVALID = -1,      /* null pointer, bad dimension or inconsistent argument */
+  KDA_ERR_UNSUPPORTED = -2,  /* chunk != 64, K or V outside {64, 128}, sizes past 32-bit indexing */
+  KDA_ERR_MISALIGNED = -3,   /* a base address is not 16-byte aligned (256 for workspace) */
+  KDA_ERR_ARCH = -4,         /* current device is not compute capability 10.3 (sm_103) */
+  KDA_ERR_LAUNCH = -5,       /* a CUDA launch or tensor-map encode failed */
+  KDA_ERR_WORKSPACE = -6,    /* workspace smaller than kda_workspace_size() */
+  KDA_ERR_BAD_SEQLENS = -16, /* (device) cu_seqlens not 0..T and non-decreasing */
+  KDA_ERR_TIMEOUT = -17      /* (device) a bounded wait inside a kernel ran out */
+};
+
+enum kda_dtype { KDA_DTYPE_BF16 = 0, KDA_DTYPE_FP32 = 1 };
+
+/* Arguments of kda_chunk_fwd and kda_fwd_intra (the latter ignores the state
+ * fields and o).  Output pointers that are NULL are not written. */
+typedef struct KdaArgs {
+  /* inputs (device) */
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* g;
+  const void* beta;
+  int32_t beta_dtype;          /* enum kda_dtype */
+  const int32_t* cu_seqlens;   /* NULL = fixed length */
+  int32_t N;                   /* number of packed sequences (ignored when cu_seqlens is NULL) */
+  int32_t B, T, Hq, Hv, K, V;
+  int32_t chunk;               /* must be 64 */
+  float scale;
+  const float* initial_state;  /* NULL = zeros */
+  /* outputs (device) */
+  void* o;                     /* required by kda_chunk_fwd */
+  float* final_state;          /* optional */
+  float* Aqk;                  /* optional for kda_chunk_fwd, required for kda_fwd_intra */
+  float* Akk_inv;              /* optional for kda_chunk_fwd, required for kda_fwd_intra */
+  void* W;                     /* optional for kda_chunk_fwd, required for kda_fwd_intra */
+  void* U;                     /* optional for kda_chunk_fwd, required for kda_fwd_intra */
+  float* G;                    /* optional (both entry points) */
+  /* optional instrumentation: host array of 3 cudaEvent_t, recorded on
+   * `stream` before the first kernel, after the intra-chunk kernel and after
+   * the state/output kernel (kda_chunk_fwd); NULL = no events. */
+  void* const* profile_events;
+} KdaArgs;
+
+typedef KdaArgs KdaFwdArgs;
+typedef KdaArgs KdaIntraArgs;
+
+/* Bytes of device workspace a call with these arguments needs (0 on invalid
+ * arguments).  Depends on the sizes and on whether W and U are NULL (the
+ * workspace then holds them for the state pass), never on tensor contents. */
+size_t kda_workspace_size(const KdaArgs* args);
+
+/* Complete chunked KDA forward: o, final_state and any requested
+ * intermediates.  Steps 1-5 above; the varlen chunk table is built on the
+ * device (as kda_prepare_chunk_indices does) inside the workspace.  The pages'
+ * own combined forward is cuLA PR #131 (Summary, sequence diagram: intra ->
+ * inverse -> W/U) followed by the delta-H and output kernels of cuLA
+ * REPO_LAYOUT.md. */
+int kda_chunk_fwd(const KdaArgs* args, void* workspace, size_t workspace_bytes, kda_stream_t stream);
+
+/* The standalone intra-chunk primitive (cuLA PR #135, which exposes
+ * chunk_kda_fwd_intra): steps 1-4 only, writing Aqk, Akk_inv, W, U (all
+ * required) and G (optional). */
+int kda_fwd_intra(const KdaArgs* args, void* workspace, size_t workspace_bytes, kda_stream_t stream);
+
+/* Varlen chunk metadata on the device (cuLA PR #135, cula/ops/kda/index.py:
+ * prepare_chunk_indices).  From cu_seqlens (device int32 [N+1]) writes
+ *   chunk_indices  (device int32 [T/chunk + N, 2]): pairs (sequence, chunk
+ *                  within sequence) in sequence order; rows >= num_chunks are
+ *                  left untouched;
+ *   chunk_offsets  (device int32 [N+1]): offsets[n] = chunks in sequences < n;
+ *   num_chunks     (device int32 [1]);
+ *   status         (device int32 [1]): set to KDA_ERR_BAD_SEQLENS (and
+ *                  num_chunks to 0) when cu[0] != 0, cu is decreasing
+ *                  anywhere, or cu[N] != T; left unchanged otherwise.
+ * chunk <= 0 returns KDA_ERR_INVALID (the pages reject a chunk size of None,
+ * zero or below zero, cuLA PR #135 review of the index tests).  N == 0 gives
+ * num_chunks = 0 and offsets = {0}. */
+int kda_prepare_chunk_indices(const int32_t* cu_seqlens, int32_t N, int32_t T, int32_t chunk,
+                              int32_t* chunk_indices, int32_t* chunk_offsets, int32_t* num_chunks,
+                              int32_t* status, kda_stream_t stream);
+
+/* Reads the device status word at the start of `workspace` after the work
+ * enqueued on `stream` so far has finished (synchronises that stream), and
+ * stores it in *status_out (KDA_OK or a device error code).  Returns KDA_OK,
+ * or KDA_ERR_INVALID / KDA_ERR_LAUNCH when it could not read it. */
+int kda_get_device_status(const void* workspace, kda_stream_t stream, int32_t* status_out);
+
+/* Static text for a status code. */
+const char* kda_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

@@ -1,0 +1,117 @@
+"""The C ABI without compute: the library loads, exports what include/kda.h
+declares, and rejects bad arguments on the host before touching a GPU."""
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from chunked_gated_delta_03_gb300 import _lib, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _lib.load()
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "kda.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    assert _declared_functions() == sorted(_lib.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_struct_layout_matches_header(tmp_path):
+    # compile a probe against include/kda.h and compare every field offset
+    fields = [f[0] for f in _lib.KdaArgs._fields_]
+    lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "kda.h"', "int main(void) {",
+             '  printf("%zu\\n", sizeof(KdaArgs));']
+    lines += [f'  printf("%zu\\n", offsetof(KdaArgs, {f}));' for f in fields]
+    lines += ["  return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    assert got[0] == ctypes.sizeof(_lib.KdaArgs)
+    assert got[1:] == [getattr(_lib.KdaArgs, f).offset for f in fields]
+
+
+def test_status_strings(lib):
+    for code in (0, -1, -2, -3, -4, -5, -6, -16, -17):
+        s = _lib.status_string(code)
+        assert s and s != "unknown status"
+    assert _lib.status_string(12345) == "unknown status"
+
+
+def _args(**kw):
+    a = _lib.KdaArgs()
+    base = 1 << 20  # 16-byte aligned dummy addresses; never dereferenced on the host path
+    a.q, a.k, a.v, a.g, a.beta, a.o = base, base, base, base, base, base
+    a.B, a.T, a.Hq, a.Hv, a.K, a.V, a.chunk = 1, 128, 2, 2, 64, 64, 64
+    a.scale = 0.125
+    for key, val in kw.items():
+        setattr(a, key, val)
+    return a
+
+
+@pytest.mark.parametrize("kw, code", [
+    (dict(chunk=0), _lib.KDA_ERR_INVALID),
+    (dict(chunk=-64), _lib.KDA_ERR_INVALID),
+    (dict(chunk=32), _lib.KDA_ERR_UNSUPPORTED),
+    (dict(K=96), _lib.KDA_ERR_UNSUPPORTED),
+    (dict(V=256), _lib.KDA_ERR_UNSUPPORTED),
+    (dict(Hv=3), _lib.KDA_ERR_INVALID),          # Hv % Hq != 0
+    (dict(B=0), _lib.KDA_ERR_INVALID),
+    (dict(T=-1), _lib.KDA_ERR_INVALID),
+    (dict(beta_dtype=7), _lib.KDA_ERR_INVALID),
+    (dict(q=0), _lib.KDA_ERR_INVALID),
+    (dict(o=0), _lib.KDA_ERR_INVALID),
+    (dict(q=(1 << 20) + 8), _lib.KDA_ERR_MISALIGNED),
+    (dict(cu_seqlens=1 << 20, B=2, N=1), _lib.KDA_ERR_INVALID),  # varlen needs B == 1
+])
+def test_chunk_fwd_rejects_bad_arguments(lib, kw, code):
+    a = _args(**kw)
+    ws_bytes = 1 << 30
+    assert _lib.kda_chunk_fwd(a, 1 << 24, ws_bytes, 0) == code
+
+
+def test_workspace_checks(lib):
+    a = _args()
+    need = _lib.kda_workspace_size(a)
+    assert need > 0 and need % 256 == 0
+    assert _lib.kda_chunk_fwd(a, 1 << 24, need - 1, 0) == _lib.KDA_ERR_WORKSPACE
+    assert _lib.kda_chunk_fwd(a, (1 << 24) + 128, need, 0) == _lib.KDA_ERR_MISALIGNED
+    assert _lib.kda_chunk_fwd(a, 0, need, 0) == _lib.KDA_ERR_INVALID
+    assert _lib.kda_workspace_size(_args(K=96)) == 0
+
+
+def test_workspace_size_accounts_for_missing_w_u(lib):
+    with_wu = _args(W=1 << 20, U=1 << 20)
+    without = _args()
+    # the state pass needs W and U: without caller buffers they live in the workspace
+    assert _lib.kda_workspace_size(without) - _lib.kda_workspace_size(with_wu) >= 2 * 128 * 2 * 64 * 2
+
+
+def test_intra_requires_its_outputs(lib):
+    a = _args()
+    assert _lib.kda_fwd_intra(a, 1 << 24, 1 << 30, 0) == _lib.KDA_ERR_INVALID
+
+
+def test_prepare_chunk_indices_rejects_bad_chunk(lib):
+    for chunk in (0, -64):
+        assert _lib.kda_prepare_chunk_indices(1 << 20, 1, 4, chunk, 1 << 20, 1 << 20, 1 << 20, 1 << 20, 0) \
+            == _lib.KDA_ERR_INVALID

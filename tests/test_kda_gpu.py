@@ -1,0 +1,264 @@
+"""GPU parity of the CUDA path against the FP64 oracle, through the C ABI.
+
+Tolerances (floating point): o and final_state max |err| <= 2e-2 and relative
+L2 <= 5e-3 (bf16 I/O); Akk_inv and Aqk relative L2 <= 1e-4 (FP32 outputs of an
+~FP32-accurate hi/lo-split product and an FP32 inverse); W, U max |err| <=
+2e-2 and relative L2 <= 5e-3 (bf16 outputs); G relative L2 <= 1e-5 (FP32
+cumsum).  Chunk indices and offsets: bit-exact.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from chunked_gated_delta_03_gb300 import _lib, build
+from chunked_gated_delta_03_gb300 import ops
+from chunked_gated_delta_03_gb300.workloads import WORKLOADS, Workload, make_inputs
+from oracle import kda_ref as ref
+
+pytestmark = pytest.mark.gpu
+
+TOL_STATE = dict(max_abs=2e-2, rel=5e-3)
+TOL_FP32 = dict(rel=1e-4)
+TOL_G = dict(rel=1e-5)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build.build()
+    _lib.load()
+
+
+def _np(t):
+    return None if t is None else t.detach().double().cpu().numpy()
+
+
+def _oracle(inp, heads=None):
+    """FP64 oracle on the CPU copy of the inputs; with ``heads``, only those
+    value heads (each run as its own single-head problem, results stacked on
+    the head axis in the order given)."""
+    cu = None if inp["cu_seqlens"] is None else inp["cu_seqlens"].cpu().numpy()
+    if heads is None:
+        return ref.kda_chunked(_np(inp["q"]), _np(inp["k"]), _np(inp["v"]), _np(inp["g"]), _np(inp["beta"]),
+                               inp["scale"], _np(inp["initial_state"]), cu, chunk_size=64)
+    grp = inp["Hv"] // inp["Hq"]
+    parts = []
+    for hv in heads:
+        hq = hv // grp
+        h0 = inp["initial_state"]
+        parts.append(ref.kda_chunked(
+            _np(inp["q"][:, :, hq:hq + 1]), _np(inp["k"][:, :, hq:hq + 1]), _np(inp["v"][:, :, hv:hv + 1]),
+            _np(inp["g"][:, :, hv:hv + 1]), _np(inp["beta"][:, :, hv:hv + 1]), inp["scale"],
+            None if h0 is None else _np(h0[:, hv:hv + 1]), cu, chunk_size=64))
+    out = {}
+    for key in parts[0]:
+        axis = 1 if key == "final_state" else 2
+        out[key] = np.concatenate([p[key] for p in parts], axis=axis)
+    return out
+
+
+def _cuda(inp):
+    return {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+
+
+def _ours(inp, inter=True, G=False):
+    return ops.chunk_kda_fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["scale"],
+                             inp["initial_state"], inp["cu_seqlens"], output_final_state=True,
+                             return_intermediates=inter, return_G=G)
+
+
+def _check(name, got, want, max_abs=None, rel=None):
+    got = np.asarray(got, np.float64)
+    want = np.asarray(want, np.float64)
+    assert np.all(np.isfinite(got)), f"{name}: non-finite values"
+    err = np.abs(got - want)
+    nrm = np.linalg.norm(want)
+    r = np.linalg.norm(got - want) / (nrm if nrm > 0 else 1.0)
+    if max_abs is not None:
+        assert err.max() <= max_abs, f"{name}: max abs err {err.max():.3e} > {max_abs}"
+    if rel is not None:
+        assert r <= rel, f"{name}: rel L2 err {r:.3e} > {rel}"
+    return float(err.max()), float(r)
+
+
+def _compare(inp, out, want, heads=None, inter=True):
+    """Compare our outputs (optionally only value heads ``heads``) with the oracle's."""
+    o, final, im = out
+    sel = slice(None) if heads is None else list(heads)
+    _check("o", _np(o[:, :, sel]), want["o"], **TOL_STATE)
+    _check("final_state", _np(final[:, sel]), want["final_state"], **TOL_STATE)
+    if inter:
+        _check("Akk_inv", _np(im["Akk_inv"][:, :, sel]), want["Akk_inv"], **TOL_FP32)
+        _check("Aqk", _np(im["Aqk"][:, :, sel]), want["Aqk"], **TOL_FP32)
+        _check("W", _np(im["W"][:, :, sel]), want["W"], **TOL_STATE)
+        _check("U", _np(im["U"][:, :, sel]), want["U"], **TOL_STATE)
+        if "G" in im:
+            _check("G", _np(im["G"][:, :, sel]), want["G"], **TOL_G)
+
+
+SMALL_CASES = {
+    "tiny": dict(),
+    "ragged_k64_v128": dict(T=130, K=64, V=128, B=2, beta_dtype="bf16"),
+    "ragged_k128_v64": dict(T=37, K=128, V=64, B=1),
+    "gva_init": dict(T=200, Hq=2, Hv=4, K=128, V=128, initial_state=True, B=2),
+    "varlen": dict(lengths=(1, 63, 64, 65, 130, 7, 0, 200), Hq=2, Hv=2, K=128, V=128, initial_state=True,
+                   beta_dtype="bf16"),
+    "varlen_gva_k64": dict(lengths=(5, 129, 64), Hq=1, Hv=3, K=64, V=64, initial_state=True),
+}
+
+
+@pytest.mark.parametrize("case", sorted(SMALL_CASES))
+def test_small_cases_match_oracle(case):
+    inp = make_inputs(WORKLOADS["tiny"], seed=100 + len(case), **SMALL_CASES[case])
+    want = _oracle(inp)
+    out = _ours(_cuda(inp), inter=True, G=True)
+    _compare(inp, out, want, inter=True)
+
+
+def test_intra_primitive_matches_oracle_and_full_path():
+    inp = _cuda(make_inputs(WORKLOADS["tiny"], seed=7, **SMALL_CASES["varlen"]))
+    intra = ops.chunk_kda_fwd_intra(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["scale"],
+                                    inp["cu_seqlens"], return_G=True)
+    _, _, im = _ours(inp, inter=True, G=True)
+    for key in ("Aqk", "Akk_inv", "W", "U", "G"):
+        assert torch.equal(intra[key], im[key]), key
+    want = _oracle({k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()})
+    _check("Akk_inv", _np(intra["Akk_inv"]), want["Akk_inv"], **TOL_FP32)
+    _check("W", _np(intra["W"]), want["W"], **TOL_STATE)
+
+
+def test_inverse_identity_on_gpu_output():
+    inp = make_inputs(WORKLOADS["mha_1k"], T=256, B=1, Hq=4, Hv=4)
+    _, _, im = _ours(_cuda(inp), inter=True, G=True)
+    want = _oracle(inp)
+    # (I + Akk) Akk_inv = I with the oracle's Akk and the GPU's inverse
+    A = want["Akk"][0, :64, 0, :64]
+    X = _np(im["Akk_inv"])[0, :64, 0, :64]
+    assert np.abs((np.eye(64) + A) @ X - np.eye(64)).max() < 1e-4
+
+
+# --------------------------------------------------------------- workloads
+@pytest.mark.parametrize("name, heads", [
+    ("tiny", None),
+    ("mha_1k", [0, 17, 63]),
+    ("mha_8k", [0, 37]),
+    ("gva_4k", [0, 5, 63]),
+    ("varlen_16k", [0, 33]),
+])
+def test_workload_matches_oracle(name, heads):
+    w = WORKLOADS[name]
+    inp = make_inputs(w)
+    want = _oracle(inp, heads=heads)
+    out = _ours(_cuda(inp), inter=True)
+    _compare(inp, out, want, heads=heads, inter=True)
+
+
+# ------------------------------------------------------------ edge cases
+def test_chunk_indices_bit_exact():
+    for lens in ([1], [64], [65], [1, 63, 64, 65, 0, 129, 3], [0, 0], [4096, 1, 2000]):
+        cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32, device="cuda")
+        idx, off = ops.prepare_chunk_indices(cu, 64)
+        want_idx, want_off = ref.prepare_chunk_indices(cu.cpu().numpy(), 64)
+        assert np.array_equal(idx.cpu().numpy(), want_idx)
+        assert np.array_equal(off.cpu().numpy(), want_off)
+    cu = torch.tensor([0], dtype=torch.int32, device="cuda")
+    idx, off = ops.prepare_chunk_indices(cu, 64)
+    assert idx.shape == (0, 2) and off.tolist() == [0]
+
+
+def test_chunk_indices_reject_bad_metadata():
+    with pytest.raises(ValueError):
+        ops.prepare_chunk_indices(torch.tensor([0, 10, 4], dtype=torch.int32, device="cuda"), 64)
+    with pytest.raises(ValueError):
+        ops.prepare_chunk_indices(torch.tensor([3, 10], dtype=torch.int32, device="cuda"), 64)
+    for bad in (None, 0, -64):
+        with pytest.raises(ValueError):
+            ops.prepare_chunk_indices(torch.tensor([0, 4], dtype=torch.int32, device="cuda"), bad)
+
+
+def test_bad_cu_seqlens_sets_device_status():
+    inp = _cuda(make_inputs(WORKLOADS["tiny"], lengths=(100, 156)))
+    a, _ = ops.make_args(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["scale"], None,
+                         inp["cu_seqlens"])
+    o = torch.zeros(1, 256, 2, 64, dtype=torch.bfloat16, device="cuda")
+    a.o = o.data_ptr()
+    bad = torch.tensor([0, 150, 100], dtype=torch.int32, device="cuda")  # decreasing
+    a.cu_seqlens = bad.data_ptr()
+    n = _lib.kda_workspace_size(a)
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    assert _lib.kda_chunk_fwd(a, ws.data_ptr(), n, torch.cuda.current_stream().cuda_stream) == _lib.KDA_OK
+    assert ops.device_status(ws) == _lib.KDA_ERR_BAD_SEQLENS
+    assert torch.count_nonzero(o) == 0  # kernels saw the status and wrote nothing
+    # a good call on the same workspace clears the status
+    a.cu_seqlens = inp["cu_seqlens"].data_ptr()
+    assert _lib.kda_chunk_fwd(a, ws.data_ptr(), n, torch.cuda.current_stream().cuda_stream) == _lib.KDA_OK
+    assert ops.device_status(ws) == _lib.KDA_OK
+
+
+def test_empty_inputs():
+    inp = _cuda(make_inputs(WORKLOADS["tiny"], T=0, initial_state=True))
+    o, final, _ = _ours(inp, inter=False)
+    assert o.numel() == 0 and torch.equal(final, inp["initial_state"])
+    inp = _cuda(make_inputs(WORKLOADS["tiny"], lengths=(0, 0), initial_state=True))
+    o, final, _ = _ours(inp, inter=False)
+    assert torch.equal(final, inp["initial_state"])
+
+
+def test_replay_is_bitwise_deterministic():
+    inp = _cuda(make_inputs(WORKLOADS["varlen_16k"], varlen_total=4096, Hq=8, Hv=8))
+    first = _ours(inp, inter=True)
+    for _ in range(3):
+        again = _ours(inp, inter=True)
+        assert torch.equal(first[0], again[0]) and torch.equal(first[1], again[1])
+        for key in first[2]:
+            assert torch.equal(first[2][key], again[2][key]), key
+
+
+def test_two_streams_give_identical_results():
+    a = _cuda(make_inputs(WORKLOADS["mha_1k"], seed=11, B=1, Hq=16, Hv=16))
+    b = _cuda(make_inputs(WORKLOADS["gva_4k"], seed=12, T=1024, Hq=4, Hv=16))
+    ref_a, ref_b = _ours(a), _ours(b)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s1):
+        out_a = _ours(a)
+    with torch.cuda.stream(s2):
+        out_b = _ours(b)
+    torch.cuda.synchronize()
+    assert torch.equal(ref_a[0], out_a[0]) and torch.equal(ref_a[1], out_a[1])
+    assert torch.equal(ref_b[0], out_b[0]) and torch.equal(ref_b[1], out_b[1])
+
+
+def test_poisoned_workspace_does_not_leak():
+    # every workspace byte starts as a NaN pattern: results must equal a run on
+    # a zeroed workspace, bit for bit (nothing reads workspace it did not write)
+    inp = _cuda(make_inputs(WORKLOADS["tiny"], seed=5, **SMALL_CASES["varlen"]))
+    outs = []
+    for fill in (0x00, 0xFF):
+        a, (B, T, Hq, Hv, K, V, N) = ops.make_args(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+                                                   inp["scale"], inp["initial_state"], inp["cu_seqlens"])
+        o = torch.full((B, T, Hv, V), float("nan"), dtype=torch.bfloat16, device="cuda")
+        fin = torch.full((N, Hv, K, V), float("nan"), dtype=torch.float32, device="cuda")
+        a.o, a.final_state = o.data_ptr(), fin.data_ptr()
+        n = _lib.kda_workspace_size(a)
+        ws = torch.full((n,), fill, dtype=torch.uint8, device="cuda")
+        assert _lib.kda_chunk_fwd(a, ws.data_ptr(), n, torch.cuda.current_stream().cuda_stream) == 0
+        torch.cuda.synchronize()
+        outs.append((o, fin))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    assert torch.isfinite(outs[0][0].float()).all() and torch.isfinite(outs[0][1]).all()
+
+
+def test_continuation_across_calls():
+    inp = make_inputs(WORKLOADS["mha_1k"], seed=21, B=1, Hq=4, Hv=4, initial_state=True)
+    full = _ours(_cuda(inp), inter=False)
+    T1 = 384 + 17
+    seq = ("q", "k", "v", "g", "beta")
+    first = {k: (v[:, :T1] if k in seq else v) for k, v in inp.items()}
+    second = {k: (v[:, T1:] if k in seq else v) for k, v in inp.items()}
+    first["T"], second["T"] = T1, inp["T"] - T1
+    r1 = _ours(_cuda(first), inter=False)
+    second["initial_state"] = r1[1].cpu()
+    r2 = _ours(_cuda(second), inter=False)
+    _check("o", _np(r2[0]), _np(full[0])[:, T1:], **TOL_STATE)
+    _check("final_state", _np(r2[1]), _np(full[1]), **TOL_STATE)

@@ -42,6 +42,7 @@ struct StateLayout {
   static constexpr uint32_t abort_slot = tmem_slot + 4;
   static constexpr uint32_t total = abort_slot + 4;
   static constexpr uint32_t bytes = total + 1024;
+  static constexpr uint32_t tmem_cols = (192 + K <= 256) ? 256 : 512;  // P, O x2, H
   static constexpr uint32_t tx_bytes = 64 * K * 2 * 2 + 64 * 64 * 2 + K * 64 * 2 + 64 * V * 2 + K * 4;
   static_assert(bytes <= 227 * 1024, "shared memory budget");
 };
@@ -102,7 +103,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, 512);
+    tmem_alloc(tmem_slot, Lay::tmem_cols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -243,7 +244,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, Lay::tmem_cols);
   }
 }
 

@@ -1,0 +1,365 @@
+#!/usr/bin/env python
+"""Throughput of the chunked KDA forward on GB300, one JSON line on rank 0.
+
+Default workload: B=2, H=64, T=8192, K=V=128, bf16 q/k/v, fp32 g and beta,
+with the Aqk / Akk_inv / W / U intermediates written (the headline
+configuration).  A step is one kda_chunk_fwd call through the C ABI over
+inputs resident in HBM; the inputs (1.34 GB) are larger than L2 (129 MB), so
+no flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the FP64 CPU oracle, timed on the host
+
+Multi-GPU (torchrun, one process per GPU): each rank runs an independent
+replica of the workload (the path has no exchange step); `value` is the
+aggregate tokens/s over all ranks, from the max per-rank time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import multiprocessing as mp
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KDA fwd ms/call & tokens/s, B=2 H=64 T=8192 K=V=128 bf16; % of roofline"
+# cuLA PR #131 (Performance table): complete public forward, B=2 H=64,
+# T=8192, FP32 beta, CuTeDSL: 0.8564 ms on SM100/SM103 (K, V not stated).
+PAGE_MS = {"mha_8k": 0.8564}
+SMI_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+# ------------------------------------------------------------------ bytes
+def algorithmic_bytes(w, N):
+    """Bytes each kernel must move once, and the path minimum, for workload w."""
+    BT = w["B"] * w["T"]
+    Hq, Hv, K, V = w["Hq"], w["Hv"], w["K"], w["V"]
+    if w["cu_seqlens"] is None:
+        nc = w["B"] * ((w["T"] + 63) // 64)
+    else:
+        lens = np.diff(w["cu_seqlens"].cpu().numpy())
+        nc = int(np.sum((lens + 63) // 64))
+    bsz = 4 if w["beta"].dtype.itemsize == 4 else 2
+    inputs = BT * (2 * Hq * K * 2 + Hv * V * 2 + Hv * K * 4 + Hv * bsz)
+    h0 = N * Hv * K * V * 4 if w["initial_state"] is not None else 0
+    exports = BT * Hv * (64 * 4 * 2 + K * 2 + V * 2) if w["intermediates"] else 0
+    state_ops = BT * Hv * (K * 2 + 64 * 2) + nc * Hv * K * (64 * 2 + 4)     # Qs, Aqk_b, Kl^T, gamma
+    wu_internal = 0 if w["intermediates"] else BT * Hv * (K * 2 + V * 2)
+    outputs = BT * Hv * V * 2 + N * Hv * K * V * 4
+    intra = inputs + exports + wu_internal + state_ops
+    state = state_ops + BT * Hv * (K * 2 + V * 2) + h0 + outputs
+    path = inputs + h0 + outputs + exports
+    return {"intra": intra, "state": state, "path": path}
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={SMI_FIELDS}", "--format=csv,noheader,nounits", "-lms", "50",
+                 "-i", str(self.gpu)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------ CPU oracle
+def _oracle_head(args):
+    q, k, v, g, beta, h0, scale = args
+    from oracle import kda_ref as ref
+    t = time.perf_counter()
+    ref.kda_chunked(q, k, v, g, beta, scale, h0, chunk_size=64)
+    return time.perf_counter() - t
+
+
+def _head_problems(w, count):
+    """Single-(sequence, value head) slices of the workload, as FP64 numpy arrays."""
+    grp = w["Hv"] // w["Hq"]
+    f64 = lambda t: t.double().numpy()
+    probs = []
+    for j in range(count):
+        b = j % w["B"]
+        hv = (j * 7) % w["Hv"]
+        hq = hv // grp
+        h0 = None if w["initial_state"] is None else f64(w["initial_state"][b:b + 1, hv:hv + 1])
+        probs.append((f64(w["q"][b:b + 1, :, hq:hq + 1]), f64(w["k"][b:b + 1, :, hq:hq + 1]),
+                      f64(w["v"][b:b + 1, :, hv:hv + 1]), f64(w["g"][b:b + 1, :, hv:hv + 1]),
+                      f64(w["beta"][b:b + 1, :, hv:hv + 1]), h0, w["scale"]))
+    return probs
+
+
+def oracle_rate(pool, cores, w, rounds):
+    """Oracle throughput in the metric's unit (tokens/s of the whole workload):
+    `rounds` x `cores` single-head problems of T tokens, run `cores` at a time."""
+    probs = _head_problems(w, cores)
+    t0 = time.perf_counter()
+    done = 0
+    for _ in range(rounds):
+        pool.map(_oracle_head, probs)
+        done += len(probs)
+    dt = time.perf_counter() - t0
+    token_heads = done * w["T"]
+    return token_heads / dt / w["Hv"], dt, done
+
+
+def make_pool():
+    os.environ.setdefault("OMP_NUM_THREADS", "1")
+    os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+    os.environ.setdefault("MKL_NUM_THREADS", "1")
+    cores = len(os.sched_getaffinity(0))
+    return mp.get_context("spawn").Pool(cores), cores
+
+
+# ------------------------------------------------------------------ main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="mha_8k")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    args = ap.parse_args()
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.warmup < 3:
+        args.warmup = 3
+
+    from chunked_gated_delta_03_gb300.workloads import WORKLOADS, make_inputs
+    wl = WORKLOADS[args.workload]
+    config = {"workload": f"{wl.name}: B={wl.B} H={wl.Hv} (Hq={wl.Hq}) T={wl.T} K={wl.K} V={wl.V}, bf16 q/k/v, "
+                          f"fp32 g, {wl.beta_dtype} beta" + (", Aqk/Akk_inv/W/U written" if wl.intermediates else ""),
+              "B": wl.B, "T": wl.T, "Hq": wl.Hq, "Hv": wl.Hv, "K": wl.K, "V": wl.V,
+              "l2": "inputs larger than L2 (no flush needed)", "parallelism": f"replicas x{world}"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        w = make_inputs(wl)
+        w["intermediates"] = wl.intermediates
+        pool, cores = make_pool()
+        for _ in range(args.warmup):
+            oracle_rate(pool, cores, w, 1)
+        rates, secs = [], 0.0
+        for _ in range(args.steps):
+            r, dt, _ = oracle_rate(pool, cores, w, 1)
+            rates.append(r)
+            secs += dt
+        pool.close()
+        value = statistics.mean(rates)
+        line = {"metric": METRIC, "value": value, "unit": "tokens/s", "impl": "reference", "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": 1e3 * wl.B * wl.T / value, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config,
+                "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                 "sample": f"per step {cores} single-(sequence, head) problems of T={wl.T}, "
+                                           f"one per core; tokens/s of the whole workload = token-heads/s / Hv"},
+                "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    # CPU baseline pool before any CUDA work (spawned workers)
+    pool = cores = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        pool, cores = make_pool()
+
+    import torch
+    import torch.distributed as dist
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from chunked_gated_delta_03_gb300 import _lib, ops
+
+    host = make_inputs(wl)
+    host["intermediates"] = wl.intermediates
+    dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in host.items()}
+    B, T, Hq, Hv, K, V, N = (host[x] for x in ("B", "T", "Hq", "Hv", "K", "V", "N"))
+    a, _ = ops.make_args(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], dev["scale"],
+                         dev["initial_state"], dev["cu_seqlens"])
+    o = torch.empty(B, T, Hv, V, dtype=torch.bfloat16, device="cuda")
+    fin = torch.empty(N, Hv, K, V, dtype=torch.float32, device="cuda")
+    outs = {"o": o, "final_state": fin}
+    a.o, a.final_state = o.data_ptr(), fin.data_ptr()
+    if wl.intermediates:
+        for name, shape, dt in (("Aqk", (B, T, Hv, 64), torch.float32), ("Akk_inv", (B, T, Hv, 64), torch.float32),
+                                ("W", (B, T, Hv, K), torch.bfloat16), ("U", (B, T, Hv, V), torch.bfloat16)):
+            outs[name] = torch.empty(shape, dtype=dt, device="cuda")
+            setattr(a, name, outs[name].data_ptr())
+    ws_bytes = _lib.kda_workspace_size(a)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+
+    def step(ev=None):
+        a.profile_events = ev
+        rc = _lib.kda_chunk_fwd(a, ws.data_ptr(), ws_bytes, sh)
+        if rc != 0:
+            raise RuntimeError(f"kda_chunk_fwd: {_lib.status_string(rc)}")
+
+    # per-step kernel events: [start, after intra, after state]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    for trio in evs:
+        for e in trio:
+            e.record(stream)
+    handles = []
+    for trio in evs:
+        arr = (ctypes.c_void_p * 3)(*[e.cuda_event for e in trio])
+        handles.append(arr)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(ctypes.cast(handles[i], ctypes.c_void_p))
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    st = ops.device_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status after the timed region: {_lib.status_string(st)}")
+    ms = t_start.elapsed_time(t_end) / args.steps
+    intra_ms = statistics.mean(evs[i][0].elapsed_time(evs[i][1]) for i in range(args.steps))
+    state_ms = statistics.mean(evs[i][1].elapsed_time(evs[i][2]) for i in range(args.steps))
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * B * T / (ms * 1e-3)
+
+    # ---- end to end through the same C call, from/to pinned host memory
+    e2e = None
+    if rank == 0:
+        pin = {k: host[k].pin_memory() for k in ("q", "k", "v", "g", "beta")}
+        if host["initial_state"] is not None:
+            pin["initial_state"] = host["initial_state"].pin_memory()
+        back = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in outs.items()}
+        h2d = sum(t.numel() * t.element_size() for t in pin.values())
+        d2h = sum(t.numel() * t.element_size() for t in back.values())
+
+        def e2e_step():
+            for k, t in pin.items():
+                dev[k].copy_(t, non_blocking=True)
+            step()
+            for k, t in back.items():
+                t.copy_(outs[k], non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+        e2e = {"value": B * T / (e2e_ms * 1e-3), "unit": "tokens/s", "ms_per_step": e2e_ms,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    hbm, bf16, src = _peaks()
+    by = algorithmic_bytes(host, N)
+    kern = {"intra": intra_ms, "state": state_ms}
+    top = max(kern, key=kern.get)
+    achieved = by[top] / (kern[top] * 1e-3) / 1e9
+    roof = {"kernel": f"kda::{top}_kernel", "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+            "frac": achieved / hbm, "traffic": None, "peak_source": src,
+            "algorithmic_bytes_per_launch": by[top]}
+    path_gbs = by["path"] / (ms * 1e-3) / 1e9
+    path = {"bytes_per_step": by["path"], "achieved": path_gbs, "peak": hbm, "unit": "GB/s",
+            "frac": path_gbs / hbm, "roofline_ms": by["path"] / (hbm * 1e9) * 1e3}
+
+    cpu = None
+    if pool is not None:
+        r, dt, done = oracle_rate(pool, cores, host, 2)
+        pool.close()
+        cpu = {"value": r, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": f"{done} single-(sequence, head) problems of T={T} ({dt:.1f} s on {cores} cores); "
+                         f"tokens/s of the whole workload = token-heads/s / Hv"}
+
+    page = PAGE_MS.get(wl.name)
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": (value / (B * T / (page * 1e-3))) if page else None,
+            "dtype": "bf16", "data": "synthetic", "config": config,
+            "kernels_ms": kern, "roofline": roof, "path_roofline": path, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": args.steps * (2 + (1 if host["cu_seqlens"] is not None else 0)),
+            "clocks": clocks}
+    print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -130,8 +130,9 @@ int check_arch() {
   return (major == 10 && minor == 3) ? KDA_OK : KDA_ERR_ARCH;
 }
 
-int check_inputs(const KdaArgs* a, const void* ws) {
-  if (!a->q || !a->k || !a->v || !a->g || !a->beta) return KDA_ERR_INVALID;
+// Inputs may be NULL only when there are no tokens (empty tensors have no storage).
+int check_inputs(const KdaArgs* a, const void* ws, long long BT) {
+  if (BT > 0 && (!a->q || !a->k || !a->v || !a->g || !a->beta)) return KDA_ERR_INVALID;
   const void* ptrs[] = {a->q, a->k, a->v, a->g, a->beta, a->cu_seqlens, a->initial_state, a->o,
                         a->final_state, a->Aqk, a->Akk_inv, a->W, a->U, a->G};
   for (const void* p : ptrs)
@@ -165,12 +166,15 @@ Problem make_problem(const Shape& s, const KdaArgs* a, uint8_t* ws, const Layout
 }
 
 // Shared front half of both entry points: checks, status reset, chunk table.
+// `full`: kda_chunk_fwd (needs o); otherwise kda_fwd_intra (needs its four
+// outputs).  Outputs may be NULL only when there are no tokens.
 int prologue(const KdaArgs* a, void* workspace, size_t ws_bytes, cudaStream_t st, bool full, Shape* s,
              Layout* L) {
   int rc = check_shape(a, s);
   if (rc) return rc;
   if (!workspace) return KDA_ERR_INVALID;
-  rc = check_inputs(a, workspace);
+  if (s->BT > 0 && (full ? !a->o : (!a->Aqk || !a->Akk_inv || !a->W || !a->U))) return KDA_ERR_INVALID;
+  rc = check_inputs(a, workspace, s->BT);
   if (rc) return rc;
   *L = make_layout(*s, a, full);
   if (ws_bytes < L->total) return KDA_ERR_WORKSPACE;
@@ -215,7 +219,6 @@ extern "C" int kda_chunk_fwd(const KdaArgs* a, void* workspace, size_t ws_bytes,
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   Shape s;
   Layout L;
-  if (a && !a->o) return KDA_ERR_INVALID;
   int rc = prologue(a, workspace, ws_bytes, st, true, &s, &L);
   if (rc) return rc;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -266,7 +269,6 @@ extern "C" int kda_fwd_intra(const KdaArgs* a, void* workspace, size_t ws_bytes,
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   Shape s;
   Layout L;
-  if (a && (!a->Aqk || !a->Akk_inv || !a->W || !a->U)) return KDA_ERR_INVALID;
   int rc = prologue(a, workspace, ws_bytes, st, false, &s, &L);
   if (rc) return rc;
   if (s.BT == 0 || s.nc_max == 0) return KDA_OK;

@@ -2,8 +2,10 @@
 
 Tolerances (floating point): o and final_state max |err| <= 2e-2 and relative
 L2 <= 5e-3 (bf16 I/O); Akk_inv and Aqk relative L2 <= 1e-4 (FP32 outputs of an
-~FP32-accurate hi/lo-split product and an FP32 inverse); W, U max |err| <=
-2e-2 and relative L2 <= 5e-3 (bf16 outputs); G relative L2 <= 1e-5 (FP32
+~FP32-accurate hi/lo-split product and an FP32 inverse); W, U elementwise
+|err| <= 2e-2 + 1e-2 |ref| and relative L2 <= 5e-3 (bf16 outputs whose values
+reach several units: a bf16 half-ulp alone is 2^-9 |x|, and the Akk_inv and
+beta*k*e^G / beta*v operands are bf16 too); G relative L2 <= 1e-5 (FP32
 cumsum).  Chunk indices and offsets: bit-exact.
 """
 
@@ -19,6 +21,7 @@ from oracle import kda_ref as ref
 pytestmark = pytest.mark.gpu
 
 TOL_STATE = dict(max_abs=2e-2, rel=5e-3)
+TOL_WU = dict(atol=2e-2, rtol=1e-2, rel=5e-3)
 TOL_FP32 = dict(rel=1e-4)
 TOL_G = dict(rel=1e-5)
 
@@ -67,7 +70,7 @@ def _ours(inp, inter=True, G=False):
                              return_intermediates=inter, return_G=G)
 
 
-def _check(name, got, want, max_abs=None, rel=None):
+def _check(name, got, want, max_abs=None, rel=None, atol=None, rtol=None):
     got = np.asarray(got, np.float64)
     want = np.asarray(want, np.float64)
     assert np.all(np.isfinite(got)), f"{name}: non-finite values"
@@ -76,6 +79,10 @@ def _check(name, got, want, max_abs=None, rel=None):
     r = np.linalg.norm(got - want) / (nrm if nrm > 0 else 1.0)
     if max_abs is not None:
         assert err.max() <= max_abs, f"{name}: max abs err {err.max():.3e} > {max_abs}"
+    if atol is not None:
+        bound = atol + rtol * np.abs(want)
+        worst = np.max(err - bound)
+        assert worst <= 0, f"{name}: |err| exceeds {atol} + {rtol}|ref| by {worst:.3e}"
     if rel is not None:
         assert r <= rel, f"{name}: rel L2 err {r:.3e} > {rel}"
     return float(err.max()), float(r)
@@ -90,8 +97,8 @@ def _compare(inp, out, want, heads=None, inter=True):
     if inter:
         _check("Akk_inv", _np(im["Akk_inv"][:, :, sel]), want["Akk_inv"], **TOL_FP32)
         _check("Aqk", _np(im["Aqk"][:, :, sel]), want["Aqk"], **TOL_FP32)
-        _check("W", _np(im["W"][:, :, sel]), want["W"], **TOL_STATE)
-        _check("U", _np(im["U"][:, :, sel]), want["U"], **TOL_STATE)
+        _check("W", _np(im["W"][:, :, sel]), want["W"], **TOL_WU)
+        _check("U", _np(im["U"][:, :, sel]), want["U"], **TOL_WU)
         if "G" in im:
             _check("G", _np(im["G"][:, :, sel]), want["G"], **TOL_G)
 
@@ -124,7 +131,7 @@ def test_intra_primitive_matches_oracle_and_full_path():
         assert torch.equal(intra[key], im[key]), key
     want = _oracle({k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()})
     _check("Akk_inv", _np(intra["Akk_inv"]), want["Akk_inv"], **TOL_FP32)
-    _check("W", _np(intra["W"]), want["W"], **TOL_STATE)
+    _check("W", _np(intra["W"]), want["W"], **TOL_WU)
 
 
 def test_inverse_identity_on_gpu_output():

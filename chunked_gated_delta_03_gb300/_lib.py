@@ -24,7 +24,8 @@ KDA_DTYPE_BF16 = 0
 KDA_DTYPE_FP32 = 1
 
 EXPORTS = ("kda_workspace_size", "kda_chunk_fwd", "kda_fwd_intra", "kda_prepare_chunk_indices",
-           "kda_get_device_status", "kda_status_string")
+           "kda_get_device_status", "kda_status_string", "kda_chunk_fwd_static_scratch")
+KDA_STATIC_SCRATCH_BYTES = 64 << 20
 
 
 class KdaArgs(ctypes.Structure):
@@ -89,6 +90,8 @@ def load():
     lib.kda_prepare_chunk_indices.restype = ctypes.c_int
     lib.kda_get_device_status.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)]
     lib.kda_get_device_status.restype = ctypes.c_int
+    lib.kda_chunk_fwd_static_scratch.argtypes = [P, ctypes.c_void_p, ctypes.c_void_p]
+    lib.kda_chunk_fwd_static_scratch.restype = ctypes.c_int
     lib.kda_status_string.argtypes = [ctypes.c_int]
     lib.kda_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -105,6 +108,11 @@ def kda_workspace_size(args: KdaArgs) -> int:
 
 def kda_chunk_fwd(args: KdaArgs, workspace: int, workspace_bytes: int, stream: int) -> int:
     return int(load().kda_chunk_fwd(ctypes.byref(args), workspace, workspace_bytes, stream))
+
+
+def kda_chunk_fwd_static_scratch(args: KdaArgs, device_status: int, stream: int) -> int:
+    """kda_chunk_fwd on the library's fixed device scratch (no workspace, no allocation)."""
+    return int(load().kda_chunk_fwd_static_scratch(ctypes.byref(args), device_status, stream))
 
 
 def kda_fwd_intra(args: KdaArgs, workspace: int, workspace_bytes: int, stream: int) -> int:

@@ -148,6 +148,33 @@ int kda_prepare_chunk_indices(const int32_t* cu_seqlens, int32_t N, int32_t T, i
  * or KDA_ERR_INVALID / KDA_ERR_LAUNCH when it could not read it. */
 int kda_get_device_status(const void* workspace, kda_stream_t stream, int32_t* status_out);
 
+/* Bytes of the fixed device scratch behind kda_chunk_fwd_static_scratch. */
+#define KDA_STATIC_SCRATCH_BYTES ((size_t)64 << 20)
+
+/* kda_chunk_fwd without a caller-supplied workspace, for callers that cannot
+ * allocate device memory: plug-ins handed only input and output buffers by a
+ * host runtime that owns the device's memory pool, and latency-critical code
+ * that must not allocate.  The pages have no counterpart of this entry point.
+ *   - The workspace is a fixed 64 MiB (KDA_STATIC_SCRATCH_BYTES) array in the
+ *     library's device image, held on every GPU that loads the library until
+ *     the process exits.  Nothing is allocated per call.
+ *   - Problems whose kda_workspace_size(args) exceeds KDA_STATIC_SCRATCH_BYTES
+ *     are rejected with KDA_ERR_WORKSPACE before any work is enqueued (at
+ *     K = V = 128 that is about 57,000 token-heads with W and U NULL, about
+ *     103,000 with W and U supplied).
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, on the current device); make that first call before any
+ *     stream capture.
+ *   - All calls share the one array, which keeps the last call's contents:
+ *     calls whose GPU work overlaps (other streams, other host threads) race
+ *     on it and must be serialised by the caller.  Each call resets the status
+ *     word it needs before its kernels run.
+ *   - device_status (optional, device int32 [1]): receives the device status
+ *     word of this call (enqueued on `stream`), as kda_get_device_status would
+ *     read it from a workspace.
+ * Arguments, outputs and error codes are otherwise those of kda_chunk_fwd. */
+int kda_chunk_fwd_static_scratch(const KdaArgs* args, int32_t* device_status, kda_stream_t stream);
+
 /* Static text for a status code. */
 const char* kda_status_string(int status);
 

@@ -97,8 +97,12 @@ struct IntraOut {
   float* gamma;     // fp32 [nc_max, Hv, K]: e^{G_last}
 };
 
-struct IntraMaps {
-  CUtensorMap q, k, v, g;
+struct IntraInputs {
+  const void* q;     // bf16 [BT, Hq, K]
+  const void* k;     // bf16 [BT, Hq, K]
+  const void* v;     // bf16 [BT, Hv, V]
+  const float* g;    // fp32 [BT, Hv, K]
+  const void* beta;  // bf16 or fp32 [BT, Hv]
 };
 
 struct StateMaps {
@@ -107,8 +111,7 @@ struct StateMaps {
 
 cudaError_t launch_chunk_index(const int32_t* cu, int N, int T, int chunk, int32_t* idx, int32_t* off,
                                int32_t* nc, int32_t* status, cudaStream_t s);
-cudaError_t launch_intra(const Problem& P, const IntraMaps& maps, const void* beta, const IntraOut& out,
-                         cudaStream_t s);
+cudaError_t launch_intra(const Problem& P, const IntraInputs& in, const IntraOut& out, cudaStream_t s);
 cudaError_t launch_state(const Problem& P, const StateMaps& maps, const float* gamma, const float* h0,
                          void* o, float* hT, cudaStream_t s);
 

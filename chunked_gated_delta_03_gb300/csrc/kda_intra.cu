@@ -1,33 +1,45 @@
-// Intra-chunk kernel: one CTA per (chunk, value head).
+// Intra-chunk kernel: persistent, warp-specialised, one CTA per SM, looping
+// over work items (chunk, value head) with stride gridDim.x.
 //
 // Steps (the intra-chunk part of cuLA PR #131, Summary: the intra-chunk
-// matrices, the FP32 inverse of (I + Akk), the W/U recompute):
-//   1. TMA loads q, k (head hv / (Hv/Hq)), v, g (head hv) for the 64 rows of
-//      the chunk; rows past the chunk's L valid rows are treated as zero.
-//   2. CUDA cores: inclusive cumsum G of g down the rows (two row halves, the
-//      second offset by the first half's sum), then the gated operands
-//      Qg = q*e^G, Kg = k*e^G, Kd = k*e^{-G}, each split into bf16 hi + lo
-//      parts, written into K-major SWIZZLE_128B tiles:
-//        A1 = [Qg; Kg] (128 x K), B1 = Kd (64 x K).
-//   3. tcgen05 (M=128, N=64): D1 = A1_hi B1_hi^T + A1_hi B1_lo^T + A1_lo B1_hi^T,
-//      an ~FP32-accurate product (residual ~2^-17 relative).  Rows 0-63 of D1
-//      are Aqk / scale, rows 64-127 are Akk / beta, both before masking.
-//   4. Aqk rows: scale, causal mask (i <= r), store fp32 (optional) and a bf16
-//      copy for the state pass.  Akk rows: beta_r, strict mask (i < r), to
-//      shared memory; two warps invert (I + Akk) by forward substitution in
-//      FP32, one column of the inverse per thread.
-//   5. tcgen05 (M=128, N=64, K=64): W^T = (beta*Kg)^T Akk_inv^T and
-//      U^T = (beta*v)^T Akk_inv^T, read back per channel and stored as bf16.
-// For the state pass it also writes Qs = scale*q*e^G (bf16, token-major),
-// Kl^T = (k*e^{G_last-G})^T (bf16, per chunk) and gamma = e^{G_last} (fp32).
+// matrices, the FP32 inverse of (I + Akk), the W/U recompute), spread over
+// three warp groups so that consecutive items overlap:
+//
+//  prep  (warps 0-7, thread = channel pair x row quarter): load q, k, v, g,
+//        beta of item j straight from global memory (coalesced, all loads of a
+//        thread in flight together); inclusive cumsum G of g down the rows (the
+//        quarters exchange partial sums); gated operands Qg = q*e^G,
+//        Kg = k*e^G, Kd = k*e^{-G}, split into bf16 hi + lo and written into
+//        K-major SWIZZLE_128B tiles A1 = [Qg; Kg] (128 x K), B1 = Kd (64 x K);
+//        (beta*Kg)^T and (beta*v)^T into the A2/A3 tiles of slot j%2; the
+//        state-pass operands Qs, Kl^T, gamma (and G) straight to global memory.
+//  mma   (lane 0 of warp 8, at the top of each item): MMA1(j): D1 = A1_hi B1_hi^T + A1_hi B1_lo^T +
+//        A1_lo B1_hi^T (M=128, N=64; rows 0-63 Aqk/scale, rows 64-127 Akk/beta,
+//        ~FP32-accurate), then MMA2(j-1): W^T = (beta*Kg)^T Akk_inv^T and
+//        U^T = (beta*v)^T Akk_inv^T (M=128, N=64, K=64).
+//  epi   (warps 8-11, TMEM quadrants 0-3): W/U of item j-1 from TMEM to
+//        global; then D1(j): Aqk rows (quadrants 0,1) scaled and causally
+//        masked to global (fp32 export and the bf16 copy for the state pass),
+//        Akk rows (quadrants 2,3) beta-scaled and strictly masked into shared
+//        memory, where quadrants 2,3 invert (I + Akk) by forward substitution
+//        in FP32, one column of the inverse per thread, into the bf16 B2 tile
+//        of slot j%2 and the fp32 export.
+//
+// TMEM: D1 double-buffered at columns 0 / 64; W^T, U^T double-buffered at
+// 128 / 256 (W) and +64 (U).  Shared memory: A1/B1 (single), A2/A3 and B2
+// (two slots), the Akk tile, partial sums.  Every wait is bounded.
 #include "kda_internal.cuh"
 
 namespace kda {
 
 namespace {
 
-constexpr int kIntraThreads = 128;
+constexpr int kPrepWarps = 8;
+constexpr int kEpiWarp0 = kPrepWarps;     // warps 8..11; lane 0 of warp 8 also issues the MMAs
+constexpr int kIntraThreads = (kPrepWarps + 4) * 32;
+constexpr int kPrepThreads = kPrepWarps * 32;
 constexpr int kAkkLd = 68;  // fp32 row stride of the Akk tile (conflict-free float4 rows)
+constexpr int kRowsPerThread = 16;
 
 template <int K, int V>
 struct IntraLayout {
@@ -35,26 +47,31 @@ struct IntraLayout {
   static constexpr uint32_t A1_lo = A1_hi + 128 * K * 2;
   static constexpr uint32_t B1_hi = A1_lo + 128 * K * 2;
   static constexpr uint32_t B1_lo = B1_hi + 64 * K * 2;
-  static constexpr uint32_t A2 = B1_lo + 64 * K * 2;    // (beta*Kg)^T, 128 x 64
-  static constexpr uint32_t A3 = A2 + 128 * 64 * 2;     // (beta*v)^T, 128 x 64
-  static constexpr uint32_t stage = A3 + 128 * 64 * 2;  // TMA staging of q, k, v, g
-  static constexpr uint32_t sQ = stage;
-  static constexpr uint32_t sK = sQ + 64 * K * 2;
-  static constexpr uint32_t sV = sK + 64 * K * 2;
-  static constexpr uint32_t sG = sV + 64 * V * 2;
-  static constexpr uint32_t stage_end = sG + 64 * K * 4;
-  // reuse of the staging area after step 2
-  static constexpr uint32_t B2 = stage;                  // Akk_inv (bf16), 64 x 64
-  static constexpr uint32_t sAkk = B2 + 64 * 64 * 2;     // fp32 64 x kAkkLd
-  static constexpr uint32_t sBeta = stage_end;           // 64 floats
-  static constexpr uint32_t sPart = sBeta + 64 * 4;      // 2 x K floats
-  static constexpr uint32_t bars = sPart + 2 * K * 4;    // 3 mbarriers
-  static constexpr uint32_t tmem_slot = bars + 3 * 8;
+  static constexpr uint32_t A23 = B1_lo + 64 * K * 2;   // 2 slots x [A2 | A3], each 128 x 64
+  static constexpr uint32_t A23_slot = 2 * 128 * 64 * 2;
+  static constexpr uint32_t B2 = A23 + 2 * A23_slot;    // 2 slots x 64 x 64 bf16
+  static constexpr uint32_t B2_slot = 64 * 64 * 2;
+  static constexpr uint32_t sAkk = B2 + 2 * B2_slot;    // fp32 64 x kAkkLd
+  static constexpr uint32_t sPart = sAkk + 64 * kAkkLd * 4;  // 2 x 4 x K floats
+  static constexpr uint32_t bars = sPart + 2 * 4 * K * 4;
+  static constexpr int kBars = 14;
+  static constexpr uint32_t tmem_slot = bars + kBars * 8;
   static constexpr uint32_t abort_slot = tmem_slot + 4;
   static constexpr uint32_t total = abort_slot + 4;
   static constexpr uint32_t bytes = total + 1024;  // slack for 1024-B alignment
-  static_assert(sAkk + 64 * kAkkLd * 4 <= stage_end, "Akk tile must fit the staging area");
   static_assert(bytes <= 227 * 1024, "shared memory budget");
+};
+
+// barrier indices
+enum {
+  kOpndFull = 0,   // prep -> mma: A1/B1/A2/A3 of item j written          (256 arrivals)
+  kA1Empty = 1,    // mma -> prep: MMA1 done reading A1/B1               (commit)
+  kA23Empty = 2,   // [2] mma -> prep: MMA2 done reading A2/A3 slot      (commit)
+  kD1Full = 4,     // [2] mma -> epi: D1 ready                           (commit)
+  kD1Empty = 6,    // [2] epi -> mma: D1 read                            (128 arrivals)
+  kB2Full = 8,     // [2] epi -> mma: B2 slot written                    (64 arrivals)
+  kD2Full = 10,    // [2] mma -> epi: W^T/U^T ready                      (commit)
+  kD2Empty = 12,   // [2] epi -> mma: W^T/U^T read                       (128 arrivals)
 };
 
 __device__ __forceinline__ void split_store(uint8_t* hi_tile, uint8_t* lo_tile, uint32_t off, float a, float b) {
@@ -65,322 +82,393 @@ __device__ __forceinline__ void split_store(uint8_t* hi_tile, uint8_t* lo_tile, 
   *reinterpret_cast<__nv_bfloat162*>(lo_tile + off) = l;
 }
 
+__device__ __forceinline__ uint4 pack8(const float* f) {
+  return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                    pack_bf16x2(f[6], f[7]));
+}
+
+// Parity of the wait for the n-th completion (n >= 0) of a barrier.
+__device__ __forceinline__ uint32_t par(int n) { return uint32_t(n) & 1u; }
+
 template <int K, int V>
 __global__ void __launch_bounds__(kIntraThreads, 1)
-    intra_kernel(const Problem P, const __grid_constant__ IntraMaps maps, const void* __restrict__ beta,
+    intra_kernel(const Problem P, const void* __restrict__ qp, const void* __restrict__ kp,
+                 const void* __restrict__ vp, const float* __restrict__ gp, const void* __restrict__ beta,
                  const IntraOut out) {
   using Lay = IntraLayout<K, V>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-
-  const int hv = blockIdx.x % P.Hv;
-  const int gc = blockIdx.x / P.Hv;
   if (*reinterpret_cast<volatile int32_t*>(P.status) != 0) return;
-  const ChunkInfo ci = chunk_info(P, gc);
-  if (!ci.valid) return;
-  const int hq = hv / (P.Hv / P.Hq);
-  const int L = ci.L, t0 = ci.t0;
-  const int tid = threadIdx.x, warp = tid >> 5;
 
-  uint64_t* bar_tma = reinterpret_cast<uint64_t*>(sm + Lay::bars);
-  uint64_t* bar_mma1 = bar_tma + 1;
-  uint64_t* bar_mma2 = bar_tma + 2;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + Lay::bars);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + Lay::tmem_slot);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + Lay::abort_slot);
-  float* sBeta = reinterpret_cast<float*>(sm + Lay::sBeta);
-  float* sPart = reinterpret_cast<float*>(sm + Lay::sPart);
+  const long long n_items = (long long)P.nc_max * P.Hv;
+  const int grp = P.Hv / P.Hq;
 
   if (tid == 0) {
     *abort_flag = 0;
-    mbar_init(bar_tma, 1);
-    mbar_init(bar_mma1, 1);
-    mbar_init(bar_mma2, 1);
+    mbar_init(&bar[kOpndFull], kPrepThreads);
+    mbar_init(&bar[kA1Empty], 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bar[kA23Empty + s], 1);
+      mbar_init(&bar[kD1Full + s], 1);
+      mbar_init(&bar[kD1Empty + s], 128);
+      mbar_init(&bar[kB2Full + s], 64);
+      mbar_init(&bar[kD2Full + s], 1);
+      mbar_init(&bar[kD2Empty + s], 128);
+    }
     fence_mbar_init();
   }
-  if (warp == 0) {
-    tmem_alloc(tmem_slot, 256);
+  if (warp == kEpiWarp0) {
+    tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
-  }
-  if (tid < 64) {
-    float b = 0.f;
-    if (tid < L) {
-      const size_t e = size_t(t0 + tid) * P.Hv + hv;
-      b = P.beta_fp32 ? reinterpret_cast<const float*>(beta)[e]
-                      : __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(beta)[e]);
-    }
-    sBeta[tid] = b;
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (tid == 0) {
-    mbar_arrive_expect_tx(bar_tma, 64 * K * 2 * 2 + 64 * V * 2 + 64 * K * 4);
-    tma_load_3d(sm + Lay::sQ, &maps.q, 0, hq, t0, bar_tma);
-    tma_load_3d(sm + Lay::sK, &maps.k, 0, hq, t0, bar_tma);
-    tma_load_3d(sm + Lay::sV, &maps.v, 0, hv, t0, bar_tma);
-    tma_load_3d(sm + Lay::sG, &maps.g, 0, hv, t0, bar_tma);
-  }
-  wait_bar(bar_tma, 0, abort_flag, P.status);
-
-  // ---- step 2: cumsum and gated operands (thread = channel pair x row half)
-  const int p = tid & 63, h = tid >> 6;
-  const int c0 = 2 * p;
-  const __nv_bfloat16* sQ = reinterpret_cast<const __nv_bfloat16*>(sm + Lay::sQ);
-  const __nv_bfloat16* sK = reinterpret_cast<const __nv_bfloat16*>(sm + Lay::sK);
-  const __nv_bfloat16* sV = reinterpret_cast<const __nv_bfloat16*>(sm + Lay::sV);
-  const float* sG = reinterpret_cast<const float*>(sm + Lay::sG);
-  if (c0 < K) {
-    float2 part = make_float2(0.f, 0.f);
-    for (int i = 32 * h; i < min(L, 32 * h + 32); ++i) {
-      const float2 gv = *reinterpret_cast<const float2*>(sG + i * K + c0);
-      part.x += gv.x;
-      part.y += gv.y;
-    }
-    sPart[h * K + c0] = part.x;
-    sPart[h * K + c0 + 1] = part.y;
-  }
-  __syncthreads();
-  const size_t head_row = size_t(gc) * P.Hv + hv;  // per-chunk buffers
-  if (c0 < K) {
-    float2 G = h ? make_float2(sPart[c0], sPart[c0 + 1]) : make_float2(0.f, 0.f);
-    const float2 glast = make_float2(sPart[c0] + sPart[K + c0], sPart[c0 + 1] + sPart[K + c0 + 1]);
-    const float2 gam = make_float2(__expf(glast.x), __expf(glast.y));
-    if (out.gamma && h == 0) *reinterpret_cast<float2*>(out.gamma + head_row * K + c0) = gam;
-    uint8_t* A1h = sm + Lay::A1_hi;
-    uint8_t* A1l = sm + Lay::A1_lo;
-    uint8_t* B1h = sm + Lay::B1_hi;
-    uint8_t* B1l = sm + Lay::B1_lo;
-#pragma unroll 1
-    for (int blk = 0; blk < 4; ++blk) {
-      float a2[2][8], kl[2][8];
+  if (warp < kPrepWarps) {
+    // =============================================================== prep
+    const int p = tid & 63;                     // channel pair
+    const int quarter = tid >> 6;               // rows 16*quarter .. +15
+    const int c0 = 2 * p;
+    const bool kact = c0 < K, vact = c0 < V;
+    float* sPart = reinterpret_cast<float*>(sm + Lay::sPart);
+    int j = 0;
+    for (long long item = blockIdx.x; item < n_items; item += gridDim.x) {
+      const int hv = int(item % P.Hv);
+      const int gc = int(item / P.Hv);
+      const ChunkInfo ci = chunk_info(P, gc);
+      if (!ci.valid) continue;
+      const int hq = hv / grp;
+      const int L = ci.L, t0 = ci.t0;
+      // ---- loads (all in flight together)
+      float2 g2[kRowsPerThread];
+      uint32_t q2[kRowsPerThread], k2[kRowsPerThread], v2[kRowsPerThread];
+      float bt[kRowsPerThread];
 #pragma unroll
-      for (int jj = 0; jj < 8; ++jj) {
-        const int i = 32 * h + 8 * blk + jj;
-        float2 Qg = make_float2(0.f, 0.f), Kg = Qg, Kd = Qg;
-        float b = 0.f;
+      for (int rr = 0; rr < kRowsPerThread; ++rr) {
+        const int i = kRowsPerThread * quarter + rr;
+        g2[rr] = make_float2(0.f, 0.f);
+        q2[rr] = k2[rr] = v2[rr] = 0u;
+        bt[rr] = 0.f;
         if (i < L) {
-          const float2 gv = *reinterpret_cast<const float2*>(sG + i * K + c0);
-          G.x += gv.x;
-          G.y += gv.y;
-          const float2 q2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(sQ + i * K + c0));
-          const float2 k2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(sK + i * K + c0));
-          const float2 eG = make_float2(__expf(G.x), __expf(G.y));
-          const float2 eN = make_float2(__expf(-G.x), __expf(-G.y));
-          Qg = make_float2(q2.x * eG.x, q2.y * eG.y);
-          Kg = make_float2(k2.x * eG.x, k2.y * eG.y);
-          Kd = make_float2(k2.x * eN.x, k2.y * eN.y);
-          b = sBeta[i];
-          const size_t tok = size_t(t0 + i) * P.Hv + hv;
-          if (out.Qs)
-            *reinterpret_cast<uint32_t*>(reinterpret_cast<__nv_bfloat16*>(out.Qs) + tok * K + c0) =
-                pack_bf16x2(P.scale * Qg.x, P.scale * Qg.y);
-          if (out.G) *reinterpret_cast<float2*>(out.G + tok * K + c0) = G;
-        }
-        split_store(A1h, A1l, sw128_offset(i, c0, 128), Qg.x, Qg.y);
-        split_store(A1h, A1l, sw128_offset(64 + i, c0, 128), Kg.x, Kg.y);
-        split_store(B1h, B1l, sw128_offset(i, c0, 64), Kd.x, Kd.y);
-        a2[0][jj] = b * Kg.x;
-        a2[1][jj] = b * Kg.y;
-        kl[0][jj] = Kd.x * gam.x;
-        kl[1][jj] = Kd.y * gam.y;
-      }
-      const int col = 32 * h + 8 * blk;
-#pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        uint4 pa = make_uint4(pack_bf16x2(a2[ch][0], a2[ch][1]), pack_bf16x2(a2[ch][2], a2[ch][3]),
-                              pack_bf16x2(a2[ch][4], a2[ch][5]), pack_bf16x2(a2[ch][6], a2[ch][7]));
-        *reinterpret_cast<uint4*>(sm + Lay::A2 + sw128_offset(c0 + ch, col, 128)) = pa;
-        if (out.KlT) {
-          uint4 pk = make_uint4(pack_bf16x2(kl[ch][0], kl[ch][1]), pack_bf16x2(kl[ch][2], kl[ch][3]),
-                                pack_bf16x2(kl[ch][4], kl[ch][5]), pack_bf16x2(kl[ch][6], kl[ch][7]));
-          *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(out.KlT) + (head_row * K + c0 + ch) * 64 +
-                                    col) = pk;
+          const size_t tq = size_t(t0 + i) * P.Hq + hq, tv = size_t(t0 + i) * P.Hv + hv;
+          if (kact) {
+            g2[rr] = __ldg(reinterpret_cast<const float2*>(gp + tv * K + c0));
+            q2[rr] = __ldg(reinterpret_cast<const uint32_t*>(reinterpret_cast<const __nv_bfloat16*>(qp) + tq * K + c0));
+            k2[rr] = __ldg(reinterpret_cast<const uint32_t*>(reinterpret_cast<const __nv_bfloat16*>(kp) + tq * K + c0));
+          }
+          if (vact)
+            v2[rr] = __ldg(reinterpret_cast<const uint32_t*>(reinterpret_cast<const __nv_bfloat16*>(vp) + tv * V + c0));
+          bt[rr] = P.beta_fp32 ? __ldg(reinterpret_cast<const float*>(beta) + tv)
+                               : __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(beta)[tv]);
         }
       }
-    }
-  }
-  // (beta * v)^T
-  if (c0 < V) {
-#pragma unroll 1
-    for (int blk = 0; blk < 4; ++blk) {
-      float a3[2][8];
+      // ---- cumsum offsets across row quarters
+      float* part = sPart + (j & 1) * 4 * K;
+      if (kact) {
+        float2 s = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int jj = 0; jj < 8; ++jj) {
-        const int i = 32 * h + 8 * blk + jj;
-        float2 bv = make_float2(0.f, 0.f);
-        if (i < L) {
-          const float2 v2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(sV + i * V + c0));
-          bv = make_float2(sBeta[i] * v2.x, sBeta[i] * v2.y);
+        for (int rr = 0; rr < kRowsPerThread; ++rr) {
+          s.x += g2[rr].x;
+          s.y += g2[rr].y;
         }
-        a3[0][jj] = bv.x;
-        a3[1][jj] = bv.y;
+        *reinterpret_cast<float2*>(part + quarter * K + c0) = s;
       }
-      const int col = 32 * h + 8 * blk;
+      named_bar_sync(1, kPrepThreads);
+      float2 G = make_float2(0.f, 0.f), glast = make_float2(0.f, 0.f);
+      if (kact) {
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        uint4 pa = make_uint4(pack_bf16x2(a3[ch][0], a3[ch][1]), pack_bf16x2(a3[ch][2], a3[ch][3]),
-                              pack_bf16x2(a3[ch][4], a3[ch][5]), pack_bf16x2(a3[ch][6], a3[ch][7]));
-        *reinterpret_cast<uint4*>(sm + Lay::A3 + sw128_offset(c0 + ch, col, 128)) = pa;
+        for (int qq = 0; qq < 4; ++qq) {
+          const float2 s = *reinterpret_cast<const float2*>(part + qq * K + c0);
+          if (qq < quarter) {
+            G.x += s.x;
+            G.y += s.y;
+          }
+          glast.x += s.x;
+          glast.y += s.y;
+        }
       }
-    }
-  }
-  fence_proxy_async_smem();
-  tc_fence_before();
-  __syncthreads();
-
-  // ---- step 3: D1 = [Qg; Kg] Kd^T with the hi/lo split (TMEM columns 0-63)
-  if (tid == 0) {
-    tc_fence_after();
-    constexpr uint32_t id = idesc_bf16_f32(128, 64);
-    const uint32_t a_hi = smem_u32(sm + Lay::A1_hi), a_lo = smem_u32(sm + Lay::A1_lo);
-    const uint32_t b_hi = smem_u32(sm + Lay::B1_hi), b_lo = smem_u32(sm + Lay::B1_lo);
-    umma_kloop(tmem, a_hi, 128, b_hi, 64, K / 16, id, 0);
-    umma_kloop(tmem, a_hi, 128, b_lo, 64, K / 16, id, 1);
-    umma_kloop(tmem, a_lo, 128, b_hi, 64, K / 16, id, 1);
-    umma_commit(bar_mma1);
-  }
-  wait_bar(bar_mma1, 0, abort_flag, P.status);
-  tc_fence_after();
-
-  // ---- step 4
-  if (warp < 2) {
-    // Aqk rows r = tid (TMEM lanes 0-63)
-    const int r = tid;
-    uint32_t x[2][32];
-    tmem_ld_x32(tmem_addr(tmem, 32 * warp, 0), x[0]);
-    tmem_ld_x32(tmem_addr(tmem, 32 * warp, 32), x[1]);
-    if (r < L) {
-      const size_t tok = size_t(t0 + r) * P.Hv + hv;
-      float a[64];
+      const float2 gam = make_float2(__expf(glast.x), __expf(glast.y));
+      const size_t head_row = size_t(gc) * P.Hv + hv;
+      if (kact && quarter == 0 && out.gamma) *reinterpret_cast<float2*>(out.gamma + head_row * K + c0) = gam;
+      // ---- wait for the operand tiles to be free
+      if (j >= 1) wait_bar(&bar[kA1Empty], par(j - 1), abort_flag, P.status);
+      if (j >= 2) wait_bar(&bar[kA23Empty + (j & 1)], par((j >> 1) - 1), abort_flag, P.status);
+      uint8_t* A2 = sm + Lay::A23 + (j & 1) * Lay::A23_slot;
+      uint8_t* A3 = A2 + 128 * 64 * 2;
+      // ---- gated operands
+      if (kact) {
+        uint8_t* A1h = sm + Lay::A1_hi;
+        uint8_t* A1l = sm + Lay::A1_lo;
+        uint8_t* B1h = sm + Lay::B1_hi;
+        uint8_t* B1l = sm + Lay::B1_lo;
 #pragma unroll
-      for (int c = 0; c < 64; ++c) a[c] = (c <= r) ? P.scale * __uint_as_float(x[c >> 5][c & 31]) : 0.f;
-      if (out.Aqk) {
-        float4* dst = reinterpret_cast<float4*>(out.Aqk + tok * 64);
+        for (int half = 0; half < 2; ++half) {
+          float a2[2][8], kl[2][8];
 #pragma unroll
-        for (int c = 0; c < 16; ++c) dst[c] = make_float4(a[4 * c], a[4 * c + 1], a[4 * c + 2], a[4 * c + 3]);
+          for (int e = 0; e < 8; ++e) {
+            const int rr = 8 * half + e;
+            const int i = kRowsPerThread * quarter + rr;
+            G.x += g2[rr].x;
+            G.y += g2[rr].y;
+            const float2 q = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&q2[rr]));
+            const float2 k = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&k2[rr]));
+            const float2 eG = make_float2(__expf(G.x), __expf(G.y));
+            const float2 eN = make_float2(__expf(-G.x), __expf(-G.y));
+            const float2 Qg = make_float2(q.x * eG.x, q.y * eG.y);
+            const float2 Kg = make_float2(k.x * eG.x, k.y * eG.y);
+            const float2 Kd = make_float2(k.x * eN.x, k.y * eN.y);
+            split_store(A1h, A1l, sw128_offset(i, c0, 128), Qg.x, Qg.y);
+            split_store(A1h, A1l, sw128_offset(64 + i, c0, 128), Kg.x, Kg.y);
+            split_store(B1h, B1l, sw128_offset(i, c0, 64), Kd.x, Kd.y);
+            a2[0][e] = bt[rr] * Kg.x;
+            a2[1][e] = bt[rr] * Kg.y;
+            kl[0][e] = Kd.x * gam.x;
+            kl[1][e] = Kd.y * gam.y;
+            if (i < L) {
+              const size_t tok = size_t(t0 + i) * P.Hv + hv;
+              if (out.Qs)
+                *reinterpret_cast<uint32_t*>(reinterpret_cast<__nv_bfloat16*>(out.Qs) + tok * K + c0) =
+                    pack_bf16x2(P.scale * Qg.x, P.scale * Qg.y);
+              if (out.G) *reinterpret_cast<float2*>(out.G + tok * K + c0) = G;
+            }
+          }
+          const int col = kRowsPerThread * quarter + 8 * half;
+#pragma unroll
+          for (int ch = 0; ch < 2; ++ch) {
+            *reinterpret_cast<uint4*>(A2 + sw128_offset(c0 + ch, col, 128)) = pack8(a2[ch]);
+            if (out.KlT)
+              *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(out.KlT) + (head_row * K + c0 + ch) * 64 +
+                                        col) = pack8(kl[ch]);
+          }
+        }
       }
-      if (out.Aqk_b) {
-        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(out.Aqk_b) + tok * 64);
+      if (vact) {
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
-          dst[c] = make_uint4(pack_bf16x2(a[8 * c], a[8 * c + 1]), pack_bf16x2(a[8 * c + 2], a[8 * c + 3]),
-                              pack_bf16x2(a[8 * c + 4], a[8 * c + 5]), pack_bf16x2(a[8 * c + 6], a[8 * c + 7]));
+        for (int half = 0; half < 2; ++half) {
+          float a3[2][8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int rr = 8 * half + e;
+            const float2 v = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v2[rr]));
+            a3[0][e] = bt[rr] * v.x;
+            a3[1][e] = bt[rr] * v.y;
+          }
+          const int col = kRowsPerThread * quarter + 8 * half;
+          *reinterpret_cast<uint4*>(A3 + sw128_offset(c0, col, 128)) = pack8(a3[0]);
+          *reinterpret_cast<uint4*>(A3 + sw128_offset(c0 + 1, col, 128)) = pack8(a3[1]);
+        }
       }
+      fence_proxy_async_smem();
+      mbar_arrive(&bar[kOpndFull]);
+      ++j;
     }
   } else {
-    // Akk rows r = tid - 64 (TMEM lanes 64-127) -> shared fp32, then invert
+    // ================================================================ epi
+    const int q4 = warp & 3;        // TMEM lane quadrant
+    const int row = 32 * q4 + lane;  // TMEM lane of this thread
     float* sAkk = reinterpret_cast<float*>(sm + Lay::sAkk);
-    const int r = tid - 64;
-    uint32_t x[2][32];
-    tmem_ld_x32(tmem_addr(tmem, 32 * warp, 0), x[0]);
-    tmem_ld_x32(tmem_addr(tmem, 32 * warp, 32), x[1]);
-    const float br = sBeta[r];
-    const bool rv = r < L;
-#pragma unroll
-    for (int c = 0; c < 64; c += 4) {
-      float4 v4;
-      v4.x = (rv && c + 0 < r) ? br * __uint_as_float(x[c >> 5][(c + 0) & 31]) : 0.f;
-      v4.y = (rv && c + 1 < r) ? br * __uint_as_float(x[c >> 5][(c + 1) & 31]) : 0.f;
-      v4.z = (rv && c + 2 < r) ? br * __uint_as_float(x[c >> 5][(c + 2) & 31]) : 0.f;
-      v4.w = (rv && c + 3 < r) ? br * __uint_as_float(x[c >> 5][(c + 3) & 31]) : 0.f;
-      *reinterpret_cast<float4*>(sAkk + r * kAkkLd + c) = v4;
-    }
-    named_bar_sync(1, 64);
-    // forward substitution: thread j owns column j of X = (I + Akk)^{-1}
-    const int j = r;
-    float xs[64];
-#pragma unroll
-    for (int i = 0; i < 64; ++i) xs[i] = 0.f;
-#pragma unroll
-    for (int rr = 0; rr < 64; ++rr) {
-      float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
-      const float4* arow = reinterpret_cast<const float4*>(sAkk + rr * kAkkLd);
-#pragma unroll
-      for (int g4 = 0; g4 < (rr + 3) / 4; ++g4) {
-        const float4 a4 = arow[g4];
-        acc0 = fmaf(a4.x, xs[4 * g4 + 0], acc0);
-        acc1 = fmaf(a4.y, xs[4 * g4 + 1], acc1);
-        acc2 = fmaf(a4.z, xs[4 * g4 + 2], acc2);
-        acc3 = fmaf(a4.w, xs[4 * g4 + 3], acc3);
-      }
-      xs[rr] = (rr == j ? 1.f : 0.f) - ((acc0 + acc1) + (acc2 + acc3));
-    }
-    uint8_t* B2 = sm + Lay::B2;
-#pragma unroll
-    for (int rr = 0; rr < 64; ++rr)
-      *reinterpret_cast<__nv_bfloat16*>(B2 + sw128_offset(rr, j, 64)) = __float2bfloat16_rn(xs[rr]);
-    if (out.Akk_inv) {
-#pragma unroll
-      for (int rr = 0; rr < 64; ++rr)
-        if (rr < L) out.Akk_inv[(size_t(t0 + rr) * P.Hv + hv) * 64 + j] = xs[rr];
-    }
-    fence_proxy_async_smem();
-  }
-  tc_fence_before();
-  __syncthreads();
-
-  // ---- step 5: W^T, U^T (TMEM columns 64-127 and 128-191)
-  if (tid == 0) {
-    tc_fence_after();
+    const bool issuer = (warp == kEpiWarp0) && lane == 0;
     constexpr uint32_t id = idesc_bf16_f32(128, 64);
-    const uint32_t b2 = smem_u32(sm + Lay::B2);
-    umma_kloop(tmem + 64, smem_u32(sm + Lay::A2), 128, b2, 64, 4, id, 0);
-    umma_kloop(tmem + 128, smem_u32(sm + Lay::A3), 128, b2, 64, 4, id, 0);
-    umma_commit(bar_mma2);
-  }
-  wait_bar(bar_mma2, 0, abort_flag, P.status);
-  tc_fence_after();
-  {
-    const int row = tid;  // channel of k (W) or v (U)
-    if (32 * warp < K) {
-      uint32_t x[2][32];
-      tmem_ld_x32(tmem_addr(tmem, 32 * warp, 64), x[0]);
-      tmem_ld_x32(tmem_addr(tmem, 32 * warp, 96), x[1]);
-      __nv_bfloat16* W = reinterpret_cast<__nv_bfloat16*>(out.W);
+    // MMA1(jj): D1 = [Qg; Kg] Kd^T with the hi/lo split
+    auto mma1 = [&](int jj) {
+      wait_bar(&bar[kOpndFull], par(jj), abort_flag, P.status);
+      if (jj >= 2) wait_bar(&bar[kD1Empty + (jj & 1)], par((jj >> 1) - 1), abort_flag, P.status);
+      tc_fence_after();
+      const uint32_t a_hi = smem_u32(sm + Lay::A1_hi), a_lo = smem_u32(sm + Lay::A1_lo);
+      const uint32_t b_hi = smem_u32(sm + Lay::B1_hi), b_lo = smem_u32(sm + Lay::B1_lo);
+      const uint32_t d1 = tmem + 64 * (jj & 1);
+      umma_kloop(d1, a_hi, 128, b_hi, 64, K / 16, id, 0);
+      umma_kloop(d1, a_hi, 128, b_lo, 64, K / 16, id, 1);
+      umma_kloop(d1, a_lo, 128, b_hi, 64, K / 16, id, 1);
+      umma_commit(&bar[kD1Full + (jj & 1)]);
+      umma_commit(&bar[kA1Empty]);
+    };
+    // MMA2(jj): W^T = A2 B2^T, U^T = A3 B2^T
+    auto mma2 = [&](int jj) {
+      const int s = jj & 1;
+      wait_bar(&bar[kB2Full + s], par(jj >> 1), abort_flag, P.status);
+      if (jj >= 2) wait_bar(&bar[kD2Empty + s], par((jj >> 1) - 1), abort_flag, P.status);
+      tc_fence_after();
+      const uint32_t a2 = smem_u32(sm + Lay::A23 + s * Lay::A23_slot);
+      const uint32_t b2 = smem_u32(sm + Lay::B2 + s * Lay::B2_slot);
+      const uint32_t dW = tmem + 128 + 128 * s;
+      umma_kloop(dW, a2, 128, b2, 64, 4, id, 0);
+      umma_kloop(dW + 64, a2 + 128 * 64 * 2, 128, b2, 64, 4, id, 0);
+      umma_commit(&bar[kD2Full + s]);
+      umma_commit(&bar[kA23Empty + s]);
+    };
+    // W/U of a finished item: thread `row` is channel k (W) / v (U)
+    auto store_wu = [&](int jj, int t0, int L, int hv) {
+      const int s = jj & 1;
+      wait_bar(&bar[kD2Full + s], par(jj >> 1), abort_flag, P.status);
+      tc_fence_after();
+      const uint32_t dW = tmem + 128 + 128 * s;
 #pragma unroll
-      for (int r = 0; r < 64; ++r)
-        if (r < L) W[(size_t(t0 + r) * P.Hv + hv) * K + row] = __float2bfloat16_rn(__uint_as_float(x[r >> 5][r & 31]));
+      for (int part = 0; part < 2; ++part) {
+        const bool act = part == 0 ? (32 * q4 < K) : (32 * q4 < V);
+        const int D = part == 0 ? K : V;
+        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(part == 0 ? out.W : out.U);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t x[32];
+          tmem_ld_x32(tmem_addr(dW + 64 * part, 32 * q4, 32 * h), x);
+          if (act) {
+#pragma unroll
+            for (int r = 0; r < 32; ++r)
+              if (32 * h + r < L)
+                dst[(size_t(t0 + 32 * h + r) * P.Hv + hv) * D + row] = __float2bfloat16_rn(__uint_as_float(x[r]));
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&bar[kD2Empty + s]);
+    };
+    int j = 0;
+    int prev_t0 = 0, prev_L = 0, prev_hv = 0;
+    for (long long item = blockIdx.x; item < n_items; item += gridDim.x) {
+      const int hv = int(item % P.Hv);
+      const ChunkInfo ci = chunk_info(P, int(item / P.Hv));
+      if (!ci.valid) continue;
+      const int L = ci.L, t0 = ci.t0;
+      if (issuer) {
+        mma1(j);
+        if (j >= 1) mma2(j - 1);
+      }
+      __syncwarp();
+      if (j >= 1) store_wu(j - 1, prev_t0, prev_L, prev_hv);
+      const int s = j & 1;
+      wait_bar(&bar[kD1Full + s], par(j >> 1), abort_flag, P.status);
+      tc_fence_after();
+      const uint32_t d1 = tmem + 64 * s;
+      if (q4 < 2) {
+        // Aqk row r = row (lanes 0-63)
+        const int r = row;
+        const size_t tok = size_t(t0 + r) * P.Hv + hv;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t x[32];
+          tmem_ld_x32(tmem_addr(d1, 32 * q4, 32 * h), x);
+          if (r < L) {
+            float a[32];
+#pragma unroll
+            for (int c = 0; c < 32; ++c) a[c] = (32 * h + c <= r) ? P.scale * __uint_as_float(x[c]) : 0.f;
+            if (out.Aqk) {
+              float4* dst = reinterpret_cast<float4*>(out.Aqk + tok * 64 + 32 * h);
+#pragma unroll
+              for (int c = 0; c < 8; ++c) dst[c] = make_float4(a[4 * c], a[4 * c + 1], a[4 * c + 2], a[4 * c + 3]);
+            }
+            if (out.Aqk_b) {
+              uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(out.Aqk_b) + tok * 64 + 32 * h);
+#pragma unroll
+              for (int c = 0; c < 4; ++c) dst[c] = pack8(a + 8 * c);
+            }
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&bar[kD1Empty + s]);
+      } else {
+        // Akk row r (lanes 64-127) -> shared fp32, then invert
+        const int r = row - 64;
+        named_bar_sync(2, 64);  // previous inverse finished reading the Akk tile
+        uint32_t xa[32], xb[32];
+        tmem_ld_x32(tmem_addr(d1, 32 * q4, 0), xa);
+        tmem_ld_x32(tmem_addr(d1, 32 * q4, 32), xb);
+        tc_fence_before();
+        mbar_arrive(&bar[kD1Empty + s]);
+        const float br = P.beta_fp32 ? (r < L ? __ldg(reinterpret_cast<const float*>(beta) + size_t(t0 + r) * P.Hv + hv)
+                                              : 0.f)
+                                     : (r < L ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(beta)
+                                                                     [size_t(t0 + r) * P.Hv + hv])
+                                              : 0.f);
+#pragma unroll
+        for (int c = 0; c < 64; c += 4) {
+          float4 v4;
+          const uint32_t* src = c < 32 ? xa : xb;
+          v4.x = (c + 0 < r) ? br * __uint_as_float(src[(c + 0) & 31]) : 0.f;
+          v4.y = (c + 1 < r) ? br * __uint_as_float(src[(c + 1) & 31]) : 0.f;
+          v4.z = (c + 2 < r) ? br * __uint_as_float(src[(c + 2) & 31]) : 0.f;
+          v4.w = (c + 3 < r) ? br * __uint_as_float(src[(c + 3) & 31]) : 0.f;
+          *reinterpret_cast<float4*>(sAkk + r * kAkkLd + c) = v4;
+        }
+        named_bar_sync(3, 64);
+        // forward substitution: thread jc owns column jc of X = (I + Akk)^{-1}
+        const int jc = r;
+        float xs[64];
+#pragma unroll
+        for (int i = 0; i < 64; ++i) xs[i] = 0.f;
+#pragma unroll
+        for (int rr = 0; rr < 64; ++rr) {
+          float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+          const float4* arow = reinterpret_cast<const float4*>(sAkk + rr * kAkkLd);
+#pragma unroll
+          for (int g4 = 0; g4 < (rr + 3) / 4; ++g4) {
+            const float4 a4 = arow[g4];
+            acc0 = fmaf(a4.x, xs[4 * g4 + 0], acc0);
+            acc1 = fmaf(a4.y, xs[4 * g4 + 1], acc1);
+            acc2 = fmaf(a4.z, xs[4 * g4 + 2], acc2);
+            acc3 = fmaf(a4.w, xs[4 * g4 + 3], acc3);
+          }
+          xs[rr] = (rr == jc ? 1.f : 0.f) - ((acc0 + acc1) + (acc2 + acc3));
+        }
+        uint8_t* B2 = sm + Lay::B2 + s * Lay::B2_slot;
+#pragma unroll
+        for (int rr = 0; rr < 64; ++rr)
+          *reinterpret_cast<__nv_bfloat16*>(B2 + sw128_offset(rr, jc, 64)) = __float2bfloat16_rn(xs[rr]);
+        fence_proxy_async_smem();
+        mbar_arrive(&bar[kB2Full + s]);
+        if (out.Akk_inv) {
+#pragma unroll
+          for (int rr = 0; rr < 64; ++rr)
+            if (rr < L) out.Akk_inv[(size_t(t0 + rr) * P.Hv + hv) * 64 + jc] = xs[rr];
+        }
+      }
+      prev_t0 = t0;
+      prev_L = L;
+      prev_hv = hv;
+      ++j;
     }
-    if (32 * warp < V) {
-      uint32_t x[2][32];
-      tmem_ld_x32(tmem_addr(tmem, 32 * warp, 128), x[0]);
-      tmem_ld_x32(tmem_addr(tmem, 32 * warp, 160), x[1]);
-      __nv_bfloat16* U = reinterpret_cast<__nv_bfloat16*>(out.U);
-#pragma unroll
-      for (int r = 0; r < 64; ++r)
-        if (r < L) U[(size_t(t0 + r) * P.Hv + hv) * V + row] = __float2bfloat16_rn(__uint_as_float(x[r >> 5][r & 31]));
+    if (j >= 1) {
+      if (issuer) mma2(j - 1);
+      __syncwarp();
+      store_wu(j - 1, prev_t0, prev_L, prev_hv);
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == kEpiWarp0) {
     tc_fence_after();
-    tmem_dealloc(tmem, 256);
+    tmem_dealloc(tmem, 512);
   }
 }
 
 template <int K, int V>
-cudaError_t launch_intra_t(const Problem& P, const IntraMaps& maps, const void* beta, const IntraOut& out,
-                           cudaStream_t s) {
+cudaError_t launch_intra_t(const Problem& P, const IntraInputs& in, const IntraOut& out, cudaStream_t s) {
   constexpr uint32_t smem = IntraLayout<K, V>::bytes;
   cudaError_t e = cudaFuncSetAttribute(intra_kernel<K, V>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const long long grid = (long long)P.nc_max * P.Hv;
-  if (grid <= 0) return cudaSuccess;
-  intra_kernel<K, V><<<unsigned(grid), kIntraThreads, smem, s>>>(P, maps, beta, out);
+  const long long items = (long long)P.nc_max * P.Hv;
+  if (items <= 0) return cudaSuccess;
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const unsigned grid = unsigned(items < sms ? items : sms);
+  intra_kernel<K, V><<<grid, kIntraThreads, smem, s>>>(P, in.q, in.k, in.v, in.g, in.beta, out);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_intra(const Problem& P, const IntraMaps& maps, const void* beta, const IntraOut& out,
-                         cudaStream_t s) {
-  if (P.K == 128 && P.V == 128) return launch_intra_t<128, 128>(P, maps, beta, out, s);
-  if (P.K == 128 && P.V == 64) return launch_intra_t<128, 64>(P, maps, beta, out, s);
-  if (P.K == 64 && P.V == 128) return launch_intra_t<64, 128>(P, maps, beta, out, s);
-  if (P.K == 64 && P.V == 64) return launch_intra_t<64, 64>(P, maps, beta, out, s);
+cudaError_t launch_intra(const Problem& P, const IntraInputs& in, const IntraOut& out, cudaStream_t s) {
+  if (P.K == 128 && P.V == 128) return launch_intra_t<128, 128>(P, in, out, s);
+  if (P.K == 128 && P.V == 64) return launch_intra_t<128, 64>(P, in, out, s);
+  if (P.K == 64 && P.V == 128) return launch_intra_t<64, 128>(P, in, out, s);
+  if (P.K == 64 && P.V == 64) return launch_intra_t<64, 64>(P, in, out, s);
   return cudaErrorInvalidValue;
 }
 

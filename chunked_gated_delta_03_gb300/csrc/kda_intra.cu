@@ -52,7 +52,9 @@ struct IntraLayout {
   static constexpr uint32_t B2 = A23 + 2 * A23_slot;    // 2 slots x 64 x 64 bf16
   static constexpr uint32_t B2_slot = 64 * 64 * 2;
   static constexpr uint32_t sAkk = B2 + 2 * B2_slot;    // fp32 64 x kAkkLd
-  static constexpr uint32_t sPart = sAkk + 64 * kAkkLd * 4;  // 2 x 4 x K floats
+  static constexpr uint32_t sX = sAkk + 64 * kAkkLd * 4;    // fp32 64 x kAkkLd: Akk_inv, row-major
+  static constexpr uint32_t sT = sX + 64 * kAkkLd * 4;       // fp32 3 x 16 x 16 block temporaries
+  static constexpr uint32_t sPart = sT + 3 * 16 * 16 * 4;    // 2 x 4 x K floats
   static constexpr uint32_t bars = sPart + 2 * 4 * K * 4;
   static constexpr int kBars = 14;
   static constexpr uint32_t tmem_slot = bars + kBars * 8;
@@ -124,6 +126,11 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
   if (warp == kEpiWarp0) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
+  }
+  {
+    // blocks of Akk_inv above the diagonal are never written: zero them once
+    float* sX = reinterpret_cast<float*>(sm + Lay::sX);
+    for (int e = tid; e < 64 * kAkkLd; e += blockDim.x) sX[e] = 0.f;
   }
   tc_fence_before();
   __syncthreads();
@@ -309,21 +316,19 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
       wait_bar(&bar[kD2Full + s], par(jj >> 1), abort_flag, P.status);
       tc_fence_after();
       const uint32_t dW = tmem + 128 + 128 * s;
-#pragma unroll
+#pragma unroll 1
       for (int part = 0; part < 2; ++part) {
-        const bool act = part == 0 ? (32 * q4 < K) : (32 * q4 < V);
         const int D = part == 0 ? K : V;
-        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(part == 0 ? out.W : out.U);
+        const bool act = 32 * q4 < D;
+        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(part == 0 ? out.W : out.U) +
+                             (size_t(t0) * P.Hv + hv) * D + row;
+        const size_t stride = size_t(P.Hv) * D;
+        uint32_t x[64];
+        tmem_ld_x64(tmem_addr(dW + 64 * part, 32 * q4, 0), x);
+        if (act) {
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t x[32];
-          tmem_ld_x32(tmem_addr(dW + 64 * part, 32 * q4, 32 * h), x);
-          if (act) {
-#pragma unroll
-            for (int r = 0; r < 32; ++r)
-              if (32 * h + r < L)
-                dst[(size_t(t0 + 32 * h + r) * P.Hv + hv) * D + row] = __float2bfloat16_rn(__uint_as_float(x[r]));
-          }
+          for (int r = 0; r < 64; ++r)
+            if (r < L) dst[size_t(r) * stride] = __float2bfloat16_rn(__uint_as_float(x[r]));
         }
       }
       tc_fence_before();
@@ -397,36 +402,84 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
           *reinterpret_cast<float4*>(sAkk + r * kAkkLd + c) = v4;
         }
         named_bar_sync(3, 64);
-        // forward substitution: thread jc owns column jc of X = (I + Akk)^{-1}
-        const int jc = r;
-        float xs[64];
+        // X = (I + Akk)^{-1} by 16 x 16 blocks.  Diagonal blocks: forward
+        // substitution in registers, thread = (block d, column c).
+        float* sX = reinterpret_cast<float*>(sm + Lay::sX);
+        float* sT = reinterpret_cast<float*>(sm + Lay::sT);
+        {
+          const int d = r >> 4, c = r & 15, base = 16 * d;
+          float x[16];
 #pragma unroll
-        for (int i = 0; i < 64; ++i) xs[i] = 0.f;
+          for (int rr = 0; rr < 16; ++rr) {
+            const float* arow = sAkk + (base + rr) * kAkkLd + base;
+            float acc = 0.f;
 #pragma unroll
-        for (int rr = 0; rr < 64; ++rr) {
-          float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
-          const float4* arow = reinterpret_cast<const float4*>(sAkk + rr * kAkkLd);
-#pragma unroll
-          for (int g4 = 0; g4 < (rr + 3) / 4; ++g4) {
-            const float4 a4 = arow[g4];
-            acc0 = fmaf(a4.x, xs[4 * g4 + 0], acc0);
-            acc1 = fmaf(a4.y, xs[4 * g4 + 1], acc1);
-            acc2 = fmaf(a4.z, xs[4 * g4 + 2], acc2);
-            acc3 = fmaf(a4.w, xs[4 * g4 + 3], acc3);
+            for (int i = 0; i < rr; ++i) acc = fmaf(arow[i], x[i], acc);
+            x[rr] = (rr == c ? 1.f : 0.f) - acc;
           }
-          xs[rr] = (rr == jc ? 1.f : 0.f) - ((acc0 + acc1) + (acc2 + acc3));
-        }
-        uint8_t* B2 = sm + Lay::B2 + s * Lay::B2_slot;
 #pragma unroll
-        for (int rr = 0; rr < 64; ++rr)
-          *reinterpret_cast<__nv_bfloat16*>(B2 + sw128_offset(rr, jc, 64)) = __float2bfloat16_rn(xs[rr]);
+          for (int rr = 0; rr < 16; ++rr) sX[(base + rr) * kAkkLd + base + c] = x[rr];
+        }
+        named_bar_sync(3, 64);
+        // Off-diagonal blocks, one block diagonal at a time:
+        //   T = Akk[16i + r, 16j : 16i] X[16j : 16i, 16j + cols],  X_ij = -X_ii T.
+        // Thread = (row r16, column quad cq) of each 16 x 16 block.
+        const int r16 = r >> 2, cq = 4 * (r & 3);
+#pragma unroll 1
+        for (int lvl = 1; lvl < 4; ++lvl) {
+#pragma unroll 1
+          for (int jb = 0; jb + lvl < 4; ++jb) {
+            const int ib = jb + lvl;
+            const float* arow = sAkk + (16 * ib + r16) * kAkkLd;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+            for (int kk = 16 * jb; kk < 16 * ib; ++kk) {
+              const float a = arow[kk];
+              const float4 xv = *reinterpret_cast<const float4*>(sX + kk * kAkkLd + 16 * jb + cq);
+              acc.x = fmaf(a, xv.x, acc.x);
+              acc.y = fmaf(a, xv.y, acc.y);
+              acc.z = fmaf(a, xv.z, acc.z);
+              acc.w = fmaf(a, xv.w, acc.w);
+            }
+            *reinterpret_cast<float4*>(sT + (jb * 16 + r16) * 16 + cq) = acc;
+          }
+          named_bar_sync(3, 64);
+#pragma unroll 1
+          for (int jb = 0; jb + lvl < 4; ++jb) {
+            const int ib = jb + lvl;
+            const float* xrow = sX + (16 * ib + r16) * kAkkLd + 16 * ib;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk) {
+              const float xv = xrow[kk];
+              const float4 t = *reinterpret_cast<const float4*>(sT + (jb * 16 + kk) * 16 + cq);
+              acc.x = fmaf(xv, t.x, acc.x);
+              acc.y = fmaf(xv, t.y, acc.y);
+              acc.z = fmaf(xv, t.z, acc.z);
+              acc.w = fmaf(xv, t.w, acc.w);
+            }
+            *reinterpret_cast<float4*>(sX + (16 * ib + r16) * kAkkLd + 16 * jb + cq) =
+                make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+          }
+          named_bar_sync(3, 64);
+        }
+        // row r of X: bf16 B2 operand row and the fp32 export row
+        uint8_t* B2 = sm + Lay::B2 + s * Lay::B2_slot;
+        const float* xr = sX + r * kAkkLd;
+        float* inv_row = (out.Akk_inv && r < L) ? out.Akk_inv + (size_t(t0 + r) * P.Hv + hv) * 64 : nullptr;
+#pragma unroll
+        for (int c8 = 0; c8 < 64; c8 += 8) {
+          const float4 u = *reinterpret_cast<const float4*>(xr + c8);
+          const float4 w = *reinterpret_cast<const float4*>(xr + c8 + 4);
+          const float f[8] = {u.x, u.y, u.z, u.w, w.x, w.y, w.z, w.w};
+          *reinterpret_cast<uint4*>(B2 + sw128_offset(r, c8, 64)) = pack8(f);
+          if (inv_row) {
+            *reinterpret_cast<float4*>(inv_row + c8) = u;
+            *reinterpret_cast<float4*>(inv_row + c8 + 4) = w;
+          }
+        }
         fence_proxy_async_smem();
         mbar_arrive(&bar[kB2Full + s]);
-        if (out.Akk_inv) {
-#pragma unroll
-          for (int rr = 0; rr < 64; ++rr)
-            if (rr < L) out.Akk_inv[(size_t(t0 + rr) * P.Hv + hv) * 64 + jc] = xs[rr];
-        }
       }
       prev_t0 = t0;
       prev_L = L;

@@ -5,17 +5,18 @@
 //
 // Everything is computed transposed so that every MMA has M = 128 (the value
 // channel v, one TMEM lane per v) and all operands are K-major SWIZZLE_128B:
-//   P^T  = S^T W^T                  (M=128 v, N=64 rows, K=K)     TMEM cols   0..63
-//   O^T  = S^T Qs^T + Delta^T Aqk^T (M=128 v, N=64 rows, K=K, 64) TMEM cols  64..191 (2 buffers)
-//   H^T  = Delta^T Kl               (M=128 v, N=K,       K=64)    TMEM cols 192..
+//   [P^T | O^T] = S^T [W; Qs]^T     (M=128 v, N=128, K=K)   TMEM cols 128b .. 128b+127 (2 buffers)
+//   O^T += Delta^T Aqk^T            (M=128 v, N=64,  K=64)  TMEM cols 128b+64 ..
+//   H^T  = Delta^T Kl               (M=128 v, N=K,   K=64)  TMEM cols 256 ..
 // with Delta = U - W S (rows past the chunk's L valid rows forced to 0),
 // Qs = scale q e^G, Kl = k e^{G_last - G}, and the update
 //   S <- Diag(e^{G_last}) S + Kl^T Delta.
 // Epilogue thread v keeps column v of S (K fp32 values) in registers and
 // writes its bf16 copy as row v of the A operand S^T for the next chunk.
 //
-// Warp roles: warp 0 issues TMA loads into a 2-stage ring, warp 1 issues the
-// MMAs, warps 2-5 (128 threads) run the epilogue.
+// Warp roles: warp 0 issues TMA loads into a 2-stage ring (and L2 prefetches
+// a few chunks further ahead, so that the stage loads hit L2), warp 1 issues
+// the MMAs, warps 2-5 (128 threads) run the epilogue.
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -24,13 +25,14 @@ namespace {
 
 constexpr int kStateThreads = 192;
 constexpr int kStages = 2;
+constexpr int kPrefetchAhead = 3;  // chunks prefetched into L2 beyond the stage being loaded
 
 template <int K, int V>
 struct StateLayout {
-  // one pipeline stage
-  static constexpr uint32_t W = 0;                        // 64 x K, K-major SW128
-  static constexpr uint32_t Qs = W + 64 * K * 2;          // 64 x K
-  static constexpr uint32_t Aqk = Qs + 64 * K * 2;        // 64 x 64
+  // one pipeline stage.  W and Qs form one 128-row B operand [W; Qs]: atom a
+  // (columns 64a..64a+63) holds the 64 W rows then the 64 Qs rows.
+  static constexpr uint32_t WQ = 0;                       // 128 x K, K-major SW128
+  static constexpr uint32_t Aqk = WQ + 128 * K * 2;       // 64 x 64
   static constexpr uint32_t Kl = Aqk + 64 * 64 * 2;       // K x 64 (Kl^T rows = k)
   static constexpr uint32_t U = Kl + K * 64 * 2;          // 64 x V, plain row-major
   static constexpr uint32_t gam = U + 64 * V * 2;         // K floats
@@ -42,7 +44,7 @@ struct StateLayout {
   static constexpr uint32_t abort_slot = tmem_slot + 4;
   static constexpr uint32_t total = abort_slot + 4;
   static constexpr uint32_t bytes = total + 1024;
-  static constexpr uint32_t tmem_cols = (192 + K <= 256) ? 256 : 512;  // P, O x2, H
+  static constexpr uint32_t tmem_cols = 512;  // [P|O] x2 at 0 / 128, H at 256
   static constexpr uint32_t tx_bytes = 64 * K * 2 * 2 + 64 * 64 * 2 + K * 64 * 2 + 64 * V * 2 + K * 4;
   static_assert(bytes <= 227 * 1024, "shared memory budget");
 };
@@ -114,17 +116,32 @@ __global__ void __launch_bounds__(kStateThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      auto prefetch = [&](int c) {
+        const int t0 = bos + c * kChunk;
+        const int gc = gc0 + c;
+#pragma unroll
+        for (int a = 0; a < K / 64; ++a) {
+          tma_prefetch_l2_3d(&maps.W, a * 64, hv, t0);
+          tma_prefetch_l2_3d(&maps.Qs, a * 64, hv, t0);
+        }
+        tma_prefetch_l2_3d(&maps.Aqk_b, 0, hv, t0);
+        tma_prefetch_l2_2d(&maps.KlT, 0, (gc * P.Hv + hv) * K);
+        tma_prefetch_l2_3d(&maps.U, 0, hv, t0);
+        bulk_prefetch_l2(gamma + (size_t(gc) * P.Hv + hv) * K, K * 4);
+      };
+      for (int c = 0; c < nch && c < kStages + kPrefetchAhead; ++c) prefetch(c);
       for (int c = 0; c < nch; ++c) {
         const int s = c & 1;
         if (c >= kStages) wait_bar(&empty[s], ((c >> 1) - 1) & 1, abort_flag, P.status);
+        if (c + kStages + kPrefetchAhead < nch) prefetch(c + kStages + kPrefetchAhead);
         uint8_t* st = sm + s * Lay::stage_bytes;
         const int t0 = bos + c * kChunk;
         const int gc = gc0 + c;
         mbar_arrive_expect_tx(&full[s], Lay::tx_bytes);
 #pragma unroll
         for (int a = 0; a < K / 64; ++a) {
-          tma_load_3d(st + Lay::W + a * 64 * 128, &maps.W, a * 64, hv, t0, &full[s]);
-          tma_load_3d(st + Lay::Qs + a * 64 * 128, &maps.Qs, a * 64, hv, t0, &full[s]);
+          tma_load_3d(st + Lay::WQ + a * 128 * 128, &maps.W, a * 64, hv, t0, &full[s]);
+          tma_load_3d(st + Lay::WQ + a * 128 * 128 + 64 * 128, &maps.Qs, a * 64, hv, t0, &full[s]);
         }
         tma_load_3d(st + Lay::Aqk, &maps.Aqk_b, 0, hv, t0, &full[s]);
         tma_load_2d(st + Lay::Kl, &maps.KlT, 0, (gc * P.Hv + hv) * K, &full[s]);
@@ -136,22 +153,22 @@ __global__ void __launch_bounds__(kStateThreads, 1)
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t id64 = idesc_bf16_f32(128, 64);
+      constexpr uint32_t id128 = idesc_bf16_f32(128, 128);
       constexpr uint32_t idK = idesc_bf16_f32(128, K);
       const uint32_t sS = smem_u32(sm + Lay::S), sD = smem_u32(sm + Lay::D);
       for (int c = 0; c < nch; ++c) {
         const int s = c & 1;
         const uint32_t st = smem_u32(sm + s * Lay::stage_bytes);
-        const uint32_t ocol = 64 + 64 * (c & 1);
+        const uint32_t pcol = 128 * (c & 1), ocol = pcol + 64;
         wait_bar(&full[s], (c >> 1) & 1, abort_flag, P.status);
         wait_bar(sready, c & 1, abort_flag, P.status);
         tc_fence_after();
-        umma_kloop(tmem + 0, sS, 128, st + Lay::W, 64, K / 16, id64, 0);
-        umma_kloop(tmem + ocol, sS, 128, st + Lay::Qs, 64, K / 16, id64, 0);
+        umma_kloop(tmem + pcol, sS, 128, st + Lay::WQ, 128, K / 16, id128, 0);
         umma_commit(bar_P);
         wait_bar(dready, c & 1, abort_flag, P.status);
         tc_fence_after();
         umma_kloop(tmem + ocol, sD, 128, st + Lay::Aqk, 64, 4, id64, 1);
-        umma_kloop(tmem + 192, sD, 128, st + Lay::Kl, K, 4, idK, 0);
+        umma_kloop(tmem + 256, sD, 128, st + Lay::Kl, K, 4, idK, 0);
         umma_commit(bar_H);
         umma_commit(&empty[s]);
       }
@@ -175,28 +192,27 @@ __global__ void __launch_bounds__(kStateThreads, 1)
       const uint8_t* st = sm + s * Lay::stage_bytes;
       const int t0 = bos + c * kChunk;
       const int L = min(kChunk, len - c * kChunk);
-      const uint32_t ocol = 64 + 64 * (c & 1);
+      const uint32_t pcol = 128 * (c & 1), ocol = pcol + 64;
       // Delta^T row v = U[:, v] - P^T row v, rows >= L zeroed
       wait_bar(bar_P, c & 1, abort_flag, P.status);
       wait_bar(&full[s], (c >> 1) & 1, abort_flag, P.status);
       tc_fence_after();
       const __nv_bfloat16* sU = reinterpret_cast<const __nv_bfloat16*>(st + Lay::U);
+      {
+        uint32_t pr[64];
+        tmem_ld_x64(tmem_addr(tmem + pcol, 32 * q4, 0), pr);
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t pr[32];
-        tmem_ld_x32(tmem_addr(tmem, 32 * q4, 32 * half), pr);
-#pragma unroll
-        for (int j = 0; j < 32; j += 8) {
+        for (int j = 0; j < 64; j += 8) {
           float d[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
-            const int i = 32 * half + j + e;
+            const int i = j + e;
             const float u = vv ? __bfloat162float(sU[i * V + v]) : 0.f;
-            d[e] = (i < L) ? u - __uint_as_float(pr[j + e]) : 0.f;
+            d[e] = (i < L) ? u - __uint_as_float(pr[i]) : 0.f;
           }
           const uint4 pk = make_uint4(pack_bf16x2(d[0], d[1]), pack_bf16x2(d[2], d[3]),
                                       pack_bf16x2(d[4], d[5]), pack_bf16x2(d[6], d[7]));
-          *reinterpret_cast<uint4*>(sD + sw128_offset(v, 32 * half + j, 128)) = pk;
+          *reinterpret_cast<uint4*>(sD + sw128_offset(v, j, 128)) = pk;
         }
       }
       fence_proxy_async_smem();
@@ -207,11 +223,11 @@ __global__ void __launch_bounds__(kStateThreads, 1)
       tc_fence_after();
       const float* sg = reinterpret_cast<const float*>(st + Lay::gam);
 #pragma unroll
-      for (int kb = 0; kb < K / 32; ++kb) {
-        uint32_t hr[32];
-        tmem_ld_x32(tmem_addr(tmem, 32 * q4, 192 + 32 * kb), hr);
+      for (int kb = 0; kb < K / 64; ++kb) {
+        uint32_t hr[64];
+        tmem_ld_x64(tmem_addr(tmem + 256 + 64 * kb, 32 * q4, 0), hr);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) S[32 * kb + j] = fmaf(sg[32 * kb + j], S[32 * kb + j], __uint_as_float(hr[j]));
+        for (int j = 0; j < 64; ++j) S[64 * kb + j] = fmaf(sg[64 * kb + j], S[64 * kb + j], __uint_as_float(hr[j]));
       }
       store_state_row<K>(sS, v, S);
       fence_proxy_async_smem();
@@ -222,16 +238,15 @@ __global__ void __launch_bounds__(kStateThreads, 1)
       // O of this chunk sits in its own TMEM buffer; the next chunk writes the
       // other one, and the chunk after that waits for this thread's next
       // sready arrival, which comes after these loads.
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t orow[32];
-        tmem_ld_x32(tmem_addr(tmem, 32 * q4, ocol + 32 * half), orow);
+      {
+        uint32_t orow[64];
+        tmem_ld_x64(tmem_addr(tmem + ocol, 32 * q4, 0), orow);
         if (vv) {
+          __nv_bfloat16* op = o + (size_t(t0) * P.Hv + hv) * V + v;
+          const size_t ostride = size_t(P.Hv) * V;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int r = 32 * half + j;
-            if (r < L) o[(size_t(t0 + r) * P.Hv + hv) * V + v] = __float2bfloat16_rn(__uint_as_float(orow[j]));
-          }
+          for (int r = 0; r < 64; ++r)
+            if (r < L) op[size_t(r) * ostride] = __float2bfloat16_rn(__uint_as_float(orow[r]));
         }
       }
     }

@@ -192,9 +192,15 @@ int prologue(const KdaArgs* a, void* workspace, size_t ws_bytes, cudaStream_t st
   return KDA_OK;
 }
 
-int run_intra(const KdaArgs* a, const Problem& P, const IntraOut& out, cudaStream_t st) {
+int run_intra(const Shape& s, const KdaArgs* a, const Problem& P, const IntraOut& out, cudaStream_t st) {
   const IntraInputs in{a->q, a->k, a->v, a->g, a->beta};
-  return launch_intra(P, in, out, st) == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
+  IntraStoreMaps m;
+  const auto bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const auto none = CU_TENSOR_MAP_SWIZZLE_NONE;
+  if (!map_tokens(&m.W, out.W, bf, 2, s.K, s.Hv, s.BT, s.K, none) ||
+      !map_tokens(&m.U, out.U, bf, 2, s.V, s.Hv, s.BT, s.V, none))
+    return KDA_ERR_LAUNCH;
+  return launch_intra(P, in, out, m, st) == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
 }
 
 }  // namespace
@@ -239,7 +245,7 @@ extern "C" int kda_chunk_fwd(const KdaArgs* a, void* workspace, size_t ws_bytes,
   out.Aqk_b = ws + L.Aqk_b;
   out.KlT = ws + L.KlT;
   out.gamma = reinterpret_cast<float*>(ws + L.gamma);
-  rc = run_intra(a, P, out, st);
+  rc = run_intra(s, a, P, out, st);
   if (rc) return rc;
   if (ev && cudaEventRecord(ev[1], st) != cudaSuccess) return KDA_ERR_LAUNCH;
 
@@ -273,7 +279,7 @@ extern "C" int kda_fwd_intra(const KdaArgs* a, void* workspace, size_t ws_bytes,
   out.W = a->W;
   out.U = a->U;
   out.G = a->G;
-  return run_intra(a, P, out, st);
+  return run_intra(s, a, P, out, st);
 }
 
 extern "C" int kda_prepare_chunk_indices(const int32_t* cu_seqlens, int32_t N, int32_t T, int32_t chunk,

@@ -68,7 +68,7 @@ struct IntraLayout {
 enum {
   kOpndFull = 0,   // prep -> mma: A1/B1/A2/A3 of item j written          (256 arrivals)
   kA1Empty = 1,    // mma -> prep: MMA1 done reading A1/B1               (commit)
-  kA23Empty = 2,   // [2] mma -> prep: MMA2 done reading A2/A3 slot      (commit)
+  kA23Empty = 2,   // [2] epi -> prep: A2/A3 slot free (MMA2 and the W/U staging done; 1 arrival)
   kD1Full = 4,     // [2] mma -> epi: D1 ready                           (commit)
   kD1Empty = 6,    // [2] epi -> mma: D1 read                            (128 arrivals)
   kB2Full = 8,     // [2] epi -> mma: B2 slot written                    (64 arrivals)
@@ -96,7 +96,7 @@ template <int K, int V>
 __global__ void __launch_bounds__(kIntraThreads, 1)
     intra_kernel(const Problem P, const void* __restrict__ qp, const void* __restrict__ kp,
                  const void* __restrict__ vp, const float* __restrict__ gp, const void* __restrict__ beta,
-                 const IntraOut out) {
+                 const IntraOut out, const __grid_constant__ IntraStoreMaps wu_maps) {
   using Lay = IntraLayout<K, V>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -152,6 +152,29 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
       if (!ci.valid) continue;
       const int hq = hv / grp;
       const int L = ci.L, t0 = ci.t0;
+      {
+        // L2 prefetch of this thread's rows of the next item (one thread per 128-B line)
+        const long long nitem = item + gridDim.x;
+        if (nitem < n_items) {
+          const int nhv = int(nitem % P.Hv);
+          const ChunkInfo nci = chunk_info(P, int(nitem / P.Hv));
+          const int nhq = nhv / grp;
+          if (nci.valid) {
+#pragma unroll 1
+            for (int rr = 0; rr < kRowsPerThread; ++rr) {
+              const int i = kRowsPerThread * quarter + rr;
+              if (i >= nci.L) break;
+              const size_t tq = size_t(nci.t0 + i) * P.Hq + nhq, tv = size_t(nci.t0 + i) * P.Hv + nhv;
+              if (kact && (p & 15) == 0) prefetch_l2(gp + tv * K + c0);
+              if (kact && (p & 31) == 0) {
+                prefetch_l2(reinterpret_cast<const __nv_bfloat16*>(qp) + tq * K + c0);
+                prefetch_l2(reinterpret_cast<const __nv_bfloat16*>(kp) + tq * K + c0);
+              }
+              if (vact && (p & 31) == 0) prefetch_l2(reinterpret_cast<const __nv_bfloat16*>(vp) + tv * V + c0);
+            }
+          }
+        }
+      }
       // ---- loads (all in flight together)
       float2 g2[kRowsPerThread];
       uint32_t q2[kRowsPerThread], k2[kRowsPerThread], v2[kRowsPerThread];
@@ -308,31 +331,54 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
       umma_kloop(dW, a2, 128, b2, 64, 4, id, 0);
       umma_kloop(dW + 64, a2 + 128 * 64 * 2, 128, b2, 64, 4, id, 0);
       umma_commit(&bar[kD2Full + s]);
-      umma_commit(&bar[kA23Empty + s]);
     };
     // W/U of a finished item: thread `row` is channel k (W) / v (U)
+    // W/U of a finished item jj (thread `row` = channel k of W / v of U).  Full
+    // chunks go through the item's A2/A3 slot (free once MMA2(jj) is done) as
+    // row-major staging tiles written out by TMA; the slot then returns to
+    // prep.  Partial chunks take plain stores.
     auto store_wu = [&](int jj, int t0, int L, int hv) {
       const int s = jj & 1;
       wait_bar(&bar[kD2Full + s], par(jj >> 1), abort_flag, P.status);
       tc_fence_after();
       const uint32_t dW = tmem + 128 + 128 * s;
+      uint8_t* stage = sm + Lay::A23 + s * Lay::A23_slot;
+      const bool full_chunk = L == kChunk;
 #pragma unroll 1
       for (int part = 0; part < 2; ++part) {
         const int D = part == 0 ? K : V;
-        const bool act = 32 * q4 < D;
-        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(part == 0 ? out.W : out.U) +
-                             (size_t(t0) * P.Hv + hv) * D + row;
-        const size_t stride = size_t(P.Hv) * D;
         uint32_t x[64];
         tmem_ld_x64(tmem_addr(dW + 64 * part, 32 * q4, 0), x);
-        if (act) {
+        if (32 * q4 < D) {
+          if (full_chunk) {
+            __nv_bfloat16* st = reinterpret_cast<__nv_bfloat16*>(stage + part * 64 * K * 2) + row;
 #pragma unroll
-          for (int r = 0; r < 64; ++r)
-            if (r < L) dst[size_t(r) * stride] = __float2bfloat16_rn(__uint_as_float(x[r]));
+            for (int r = 0; r < 64; ++r) st[r * D] = __float2bfloat16_rn(__uint_as_float(x[r]));
+          } else {
+            __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(part == 0 ? out.W : out.U) +
+                                 (size_t(t0) * P.Hv + hv) * D + row;
+            const size_t stride = size_t(P.Hv) * D;
+#pragma unroll
+            for (int r = 0; r < 64; ++r)
+              if (r < L) dst[size_t(r) * stride] = __float2bfloat16_rn(__uint_as_float(x[r]));
+          }
         }
       }
       tc_fence_before();
       mbar_arrive(&bar[kD2Empty + s]);
+      if (full_chunk) {
+        fence_proxy_async_smem();
+        named_bar_sync(4, 128);
+      }
+      if (issuer) {
+        if (full_chunk) {
+          tma_store_3d(&wu_maps.W, stage, 0, hv, t0);
+          tma_store_3d(&wu_maps.U, stage + 64 * K * 2, 0, hv, t0);
+          bulk_commit_group();
+          bulk_wait_group_read0();
+        }
+        mbar_arrive(&bar[kA23Empty + s]);
+      }
     };
     int j = 0;
     int prev_t0 = 0, prev_L = 0, prev_hv = 0;
@@ -491,6 +537,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
       __syncwarp();
       store_wu(j - 1, prev_t0, prev_L, prev_hv);
     }
+    if (issuer) bulk_wait_group0();
   }
   tc_fence_before();
   __syncthreads();
@@ -501,7 +548,8 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
 }
 
 template <int K, int V>
-cudaError_t launch_intra_t(const Problem& P, const IntraInputs& in, const IntraOut& out, cudaStream_t s) {
+cudaError_t launch_intra_t(const Problem& P, const IntraInputs& in, const IntraOut& out, const IntraStoreMaps& maps,
+                           cudaStream_t s) {
   constexpr uint32_t smem = IntraLayout<K, V>::bytes;
   cudaError_t e = cudaFuncSetAttribute(intra_kernel<K, V>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -511,17 +559,18 @@ cudaError_t launch_intra_t(const Problem& P, const IntraInputs& in, const IntraO
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   const unsigned grid = unsigned(items < sms ? items : sms);
-  intra_kernel<K, V><<<grid, kIntraThreads, smem, s>>>(P, in.q, in.k, in.v, in.g, in.beta, out);
+  intra_kernel<K, V><<<grid, kIntraThreads, smem, s>>>(P, in.q, in.k, in.v, in.g, in.beta, out, maps);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_intra(const Problem& P, const IntraInputs& in, const IntraOut& out, cudaStream_t s) {
-  if (P.K == 128 && P.V == 128) return launch_intra_t<128, 128>(P, in, out, s);
-  if (P.K == 128 && P.V == 64) return launch_intra_t<128, 64>(P, in, out, s);
-  if (P.K == 64 && P.V == 128) return launch_intra_t<64, 128>(P, in, out, s);
-  if (P.K == 64 && P.V == 64) return launch_intra_t<64, 64>(P, in, out, s);
+cudaError_t launch_intra(const Problem& P, const IntraInputs& in, const IntraOut& out, const IntraStoreMaps& maps,
+                         cudaStream_t s) {
+  if (P.K == 128 && P.V == 128) return launch_intra_t<128, 128>(P, in, out, maps, s);
+  if (P.K == 128 && P.V == 64) return launch_intra_t<128, 64>(P, in, out, maps, s);
+  if (P.K == 64 && P.V == 128) return launch_intra_t<64, 128>(P, in, out, maps, s);
+  if (P.K == 64 && P.V == 64) return launch_intra_t<64, 64>(P, in, out, maps, s);
   return cudaErrorInvalidValue;
 }
 

@@ -14,9 +14,12 @@
 // Epilogue thread v keeps column v of S (K fp32 values) in registers and
 // writes its bf16 copy as row v of the A operand S^T for the next chunk.
 //
-// Warp roles: warp 0 issues TMA loads into a 2-stage ring (and L2 prefetches
-// a few chunks further ahead, so that the stage loads hit L2), warp 1 issues
-// the MMAs, warps 2-5 (128 threads) run the epilogue.
+// Warp roles: warp 0 issues TMA loads (and L2 prefetches a few chunks further
+// ahead, so that the stage loads hit L2), warp 1 issues the MMAs, warps 2-5
+// (128 threads) run the epilogue.  Two rings: ring A (MMA operands [W; Qs],
+// Aqk, Kl^T; 2 stages) is released by the MMAs' own completion, so the next
+// loads start mid-chunk; ring B (U and gamma, read by the epilogue; 3 stages)
+// is released by the epilogue.
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -24,28 +27,33 @@ namespace kda {
 namespace {
 
 constexpr int kStateThreads = 192;
-constexpr int kStages = 2;
+constexpr int kStagesA = 2;
+constexpr int kStagesB = 3;
 constexpr int kPrefetchAhead = 3;  // chunks prefetched into L2 beyond the stage being loaded
 
 template <int K, int V>
 struct StateLayout {
-  // one pipeline stage.  W and Qs form one 128-row B operand [W; Qs]: atom a
+  // ring A stage.  W and Qs form one 128-row B operand [W; Qs]: atom a
   // (columns 64a..64a+63) holds the 64 W rows then the 64 Qs rows.
   static constexpr uint32_t WQ = 0;                       // 128 x K, K-major SW128
   static constexpr uint32_t Aqk = WQ + 128 * K * 2;       // 64 x 64
   static constexpr uint32_t Kl = Aqk + 64 * 64 * 2;       // K x 64 (Kl^T rows = k)
-  static constexpr uint32_t U = Kl + K * 64 * 2;          // 64 x V, plain row-major
+  static constexpr uint32_t stageA_bytes = ((Kl + K * 64 * 2) + 1023) / 1024 * 1024;
+  // ring B stage
+  static constexpr uint32_t U = 0;                        // 64 x V, plain row-major
   static constexpr uint32_t gam = U + 64 * V * 2;         // K floats
-  static constexpr uint32_t stage_bytes = ((gam + K * 4) + 1023) / 1024 * 1024;
-  static constexpr uint32_t S = kStages * stage_bytes;    // 128 x K, K-major SW128 (A operand S^T)
+  static constexpr uint32_t stageB_bytes = ((gam + K * 4) + 1023) / 1024 * 1024;
+  static constexpr uint32_t ringB = kStagesA * stageA_bytes;
+  static constexpr uint32_t S = ringB + kStagesB * stageB_bytes;  // 128 x K, K-major SW128 (A operand S^T)
   static constexpr uint32_t D = S + 128 * K * 2;          // 128 x 64 (A operand Delta^T)
-  static constexpr uint32_t bars = D + 128 * 64 * 2;      // full[2], empty[2], P, H, sready, dready
-  static constexpr uint32_t tmem_slot = bars + 8 * 8;
+  static constexpr uint32_t bars = D + 128 * 64 * 2;      // fullA[2], emptyA[2], fullB[3], emptyB[3], P, H, sready, dready
+  static constexpr uint32_t tmem_slot = bars + 14 * 8;
   static constexpr uint32_t abort_slot = tmem_slot + 4;
   static constexpr uint32_t total = abort_slot + 4;
   static constexpr uint32_t bytes = total + 1024;
   static constexpr uint32_t tmem_cols = 512;  // [P|O] x2 at 0 / 128, H at 256
-  static constexpr uint32_t tx_bytes = 64 * K * 2 * 2 + 64 * 64 * 2 + K * 64 * 2 + 64 * V * 2 + K * 4;
+  static constexpr uint32_t txA_bytes = 128 * K * 2 + 64 * 64 * 2 + K * 64 * 2;
+  static constexpr uint32_t txB_bytes = 64 * V * 2 + K * 4;
   static_assert(bytes <= 227 * 1024, "shared memory budget");
 };
 
@@ -83,20 +91,26 @@ __global__ void __launch_bounds__(kStateThreads, 1)
   const int nch = (len + kChunk - 1) / kChunk;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  uint64_t* full = reinterpret_cast<uint64_t*>(sm + Lay::bars);
-  uint64_t* empty = full + 2;
-  uint64_t* bar_P = full + 4;
-  uint64_t* bar_H = full + 5;
-  uint64_t* sready = full + 6;
-  uint64_t* dready = full + 7;
+  uint64_t* fullA = reinterpret_cast<uint64_t*>(sm + Lay::bars);
+  uint64_t* emptyA = fullA + 2;
+  uint64_t* fullB = fullA + 4;
+  uint64_t* emptyB = fullA + 7;
+  uint64_t* bar_P = fullA + 10;
+  uint64_t* bar_H = fullA + 11;
+  uint64_t* sready = fullA + 12;
+  uint64_t* dready = fullA + 13;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + Lay::tmem_slot);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + Lay::abort_slot);
 
   if (tid == 0) {
     *abort_flag = 0;
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1 + 4);
+    for (int s = 0; s < kStagesA; ++s) {
+      mbar_init(&fullA[s], 1);
+      mbar_init(&emptyA[s], 1);
+    }
+    for (int s = 0; s < kStagesB; ++s) {
+      mbar_init(&fullB[s], 1);
+      mbar_init(&emptyB[s], 4);
     }
     mbar_init(bar_P, 1);
     mbar_init(bar_H, 1);
@@ -129,24 +143,28 @@ __global__ void __launch_bounds__(kStateThreads, 1)
         tma_prefetch_l2_3d(&maps.U, 0, hv, t0);
         bulk_prefetch_l2(gamma + (size_t(gc) * P.Hv + hv) * K, K * 4);
       };
-      for (int c = 0; c < nch && c < kStages + kPrefetchAhead; ++c) prefetch(c);
+      constexpr int kAhead = kStagesA + kPrefetchAhead;
+      for (int c = 0; c < nch && c < kAhead; ++c) prefetch(c);
       for (int c = 0; c < nch; ++c) {
-        const int s = c & 1;
-        if (c >= kStages) wait_bar(&empty[s], ((c >> 1) - 1) & 1, abort_flag, P.status);
-        if (c + kStages + kPrefetchAhead < nch) prefetch(c + kStages + kPrefetchAhead);
-        uint8_t* st = sm + s * Lay::stage_bytes;
+        if (c + kAhead < nch) prefetch(c + kAhead);
         const int t0 = bos + c * kChunk;
         const int gc = gc0 + c;
-        mbar_arrive_expect_tx(&full[s], Lay::tx_bytes);
+        const int sa = c % kStagesA, sb = c % kStagesB;
+        if (c >= kStagesA) wait_bar(&emptyA[sa], (c / kStagesA - 1) & 1, abort_flag, P.status);
+        uint8_t* st = sm + sa * Lay::stageA_bytes;
+        mbar_arrive_expect_tx(&fullA[sa], Lay::txA_bytes);
 #pragma unroll
         for (int a = 0; a < K / 64; ++a) {
-          tma_load_3d(st + Lay::WQ + a * 128 * 128, &maps.W, a * 64, hv, t0, &full[s]);
-          tma_load_3d(st + Lay::WQ + a * 128 * 128 + 64 * 128, &maps.Qs, a * 64, hv, t0, &full[s]);
+          tma_load_3d(st + Lay::WQ + a * 128 * 128, &maps.W, a * 64, hv, t0, &fullA[sa]);
+          tma_load_3d(st + Lay::WQ + a * 128 * 128 + 64 * 128, &maps.Qs, a * 64, hv, t0, &fullA[sa]);
         }
-        tma_load_3d(st + Lay::Aqk, &maps.Aqk_b, 0, hv, t0, &full[s]);
-        tma_load_2d(st + Lay::Kl, &maps.KlT, 0, (gc * P.Hv + hv) * K, &full[s]);
-        tma_load_3d(st + Lay::U, &maps.U, 0, hv, t0, &full[s]);
-        bulk_load(st + Lay::gam, gamma + (size_t(gc) * P.Hv + hv) * K, K * 4, &full[s]);
+        tma_load_3d(st + Lay::Aqk, &maps.Aqk_b, 0, hv, t0, &fullA[sa]);
+        tma_load_2d(st + Lay::Kl, &maps.KlT, 0, (gc * P.Hv + hv) * K, &fullA[sa]);
+        if (c >= kStagesB) wait_bar(&emptyB[sb], (c / kStagesB - 1) & 1, abort_flag, P.status);
+        uint8_t* sbp = sm + Lay::ringB + sb * Lay::stageB_bytes;
+        mbar_arrive_expect_tx(&fullB[sb], Lay::txB_bytes);
+        tma_load_3d(sbp + Lay::U, &maps.U, 0, hv, t0, &fullB[sb]);
+        bulk_load(sbp + Lay::gam, gamma + (size_t(gc) * P.Hv + hv) * K, K * 4, &fullB[sb]);
       }
     }
   } else if (warp == 1) {
@@ -157,10 +175,10 @@ __global__ void __launch_bounds__(kStateThreads, 1)
       constexpr uint32_t idK = idesc_bf16_f32(128, K);
       const uint32_t sS = smem_u32(sm + Lay::S), sD = smem_u32(sm + Lay::D);
       for (int c = 0; c < nch; ++c) {
-        const int s = c & 1;
-        const uint32_t st = smem_u32(sm + s * Lay::stage_bytes);
+        const int sa = c % kStagesA;
+        const uint32_t st = smem_u32(sm + sa * Lay::stageA_bytes);
         const uint32_t pcol = 128 * (c & 1), ocol = pcol + 64;
-        wait_bar(&full[s], (c >> 1) & 1, abort_flag, P.status);
+        wait_bar(&fullA[sa], (c / kStagesA) & 1, abort_flag, P.status);
         wait_bar(sready, c & 1, abort_flag, P.status);
         tc_fence_after();
         umma_kloop(tmem + pcol, sS, 128, st + Lay::WQ, 128, K / 16, id128, 0);
@@ -170,7 +188,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
         umma_kloop(tmem + ocol, sD, 128, st + Lay::Aqk, 64, 4, id64, 1);
         umma_kloop(tmem + 256, sD, 128, st + Lay::Kl, K, 4, idK, 0);
         umma_commit(bar_H);
-        umma_commit(&empty[s]);
+        umma_commit(&emptyA[sa]);
       }
     }
   } else {
@@ -188,14 +206,14 @@ __global__ void __launch_bounds__(kStateThreads, 1)
     fence_proxy_async_smem();
     mbar_arrive(sready);
     for (int c = 0; c < nch; ++c) {
-      const int s = c & 1;
-      const uint8_t* st = sm + s * Lay::stage_bytes;
+      const int sb = c % kStagesB;
+      const uint8_t* st = sm + Lay::ringB + sb * Lay::stageB_bytes;
       const int t0 = bos + c * kChunk;
       const int L = min(kChunk, len - c * kChunk);
       const uint32_t pcol = 128 * (c & 1), ocol = pcol + 64;
       // Delta^T row v = U[:, v] - P^T row v, rows >= L zeroed
       wait_bar(bar_P, c & 1, abort_flag, P.status);
-      wait_bar(&full[s], (c >> 1) & 1, abort_flag, P.status);
+      wait_bar(&fullB[sb], (c / kStagesB) & 1, abort_flag, P.status);
       tc_fence_after();
       const __nv_bfloat16* sU = reinterpret_cast<const __nv_bfloat16*>(st + Lay::U);
       {
@@ -234,7 +252,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
       tc_fence_before();
       mbar_arrive(sready);
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
+      if (lane == 0) mbar_arrive(&emptyB[sb]);
       // O of this chunk sits in its own TMEM buffer; the next chunk writes the
       // other one, and the chunk after that waits for this thread's next
       // sready arrival, which comes after these loads.

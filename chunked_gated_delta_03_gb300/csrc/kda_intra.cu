@@ -76,12 +76,27 @@ enum {
   kD2Empty = 12,   // [2] epi -> mma: W^T/U^T read                       (128 arrivals)
 };
 
+// 2^x by the MUFU ex2 instruction; e^x is taken as 2^(x log2 e).
+__device__ __forceinline__ float exp2f_fast(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ void split_store(uint8_t* hi_tile, uint8_t* lo_tile, uint32_t off, float a, float b) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
   const float2 hf = __bfloat1622float2(h);
   const __nv_bfloat162 l = __floats2bfloat162_rn(a - hf.x, b - hf.y);
   *reinterpret_cast<__nv_bfloat162*>(hi_tile + off) = h;
   *reinterpret_cast<__nv_bfloat162*>(lo_tile + off) = l;
+}
+
+// x = hi + lo with hi = bf16(x) and lo = bf16(x - hi), on a channel pair.
+__device__ __forceinline__ void split_store2(uint8_t* hi_tile, uint8_t* lo_tile, uint32_t off, f2 x) {
+  const uint32_t h = f2_to_bf16x2(x);
+  const f2 lo = f2_sub(x, f2_from_bf16x2(h));
+  *reinterpret_cast<uint32_t*>(hi_tile + off) = h;
+  *reinterpret_cast<uint32_t*>(lo_tile + off) = f2_to_bf16x2(lo);
 }
 
 __device__ __forceinline__ uint4 pack8(const float* f) {
@@ -233,6 +248,10 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
       uint8_t* A3 = A2 + 128 * 64 * 2;
       // ---- gated operands
       if (kact) {
+        f2 G2 = f2_make(G.x, G.y);
+        const f2 gam2 = f2_make(gam.x, gam.y);
+        const f2 scale2 = f2_make(P.scale, P.scale);
+        const f2 kLog2e2 = f2_make(1.4426950408889634f, 1.4426950408889634f);
         uint8_t* A1h = sm + Lay::A1_hi;
         uint8_t* A1l = sm + Lay::A1_lo;
         uint8_t* B1h = sm + Lay::B1_hi;
@@ -244,28 +263,31 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
           for (int e = 0; e < 8; ++e) {
             const int rr = 8 * half + e;
             const int i = kRowsPerThread * quarter + rr;
-            G.x += g2[rr].x;
-            G.y += g2[rr].y;
-            const float2 q = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&q2[rr]));
-            const float2 k = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&k2[rr]));
-            const float2 eG = make_float2(__expf(G.x), __expf(G.y));
-            const float2 eN = make_float2(__expf(-G.x), __expf(-G.y));
-            const float2 Qg = make_float2(q.x * eG.x, q.y * eG.y);
-            const float2 Kg = make_float2(k.x * eG.x, k.y * eG.y);
-            const float2 Kd = make_float2(k.x * eN.x, k.y * eN.y);
-            split_store(A1h, A1l, sw128_offset(i, c0, 128), Qg.x, Qg.y);
-            split_store(A1h, A1l, sw128_offset(64 + i, c0, 128), Kg.x, Kg.y);
-            split_store(B1h, B1l, sw128_offset(i, c0, 64), Kd.x, Kd.y);
-            a2[0][e] = bt[rr] * Kg.x;
-            a2[1][e] = bt[rr] * Kg.y;
-            kl[0][e] = Kd.x * gam.x;
-            kl[1][e] = Kd.y * gam.y;
+            G2 = f2_add(G2, f2_make(g2[rr].x, g2[rr].y));
+            const f2 q = f2_from_bf16x2(q2[rr]);
+            const f2 k = f2_from_bf16x2(k2[rr]);
+            const f2 gl = f2_mul(G2, kLog2e2);
+            const float2 glv = f2_split(gl);
+            const f2 eG = f2_make(exp2f_fast(glv.x), exp2f_fast(glv.y));
+            const f2 eN = f2_make(exp2f_fast(-glv.x), exp2f_fast(-glv.y));
+            const f2 Qg = f2_mul(q, eG);
+            const f2 Kg = f2_mul(k, eG);
+            const f2 Kd = f2_mul(k, eN);
+            split_store2(A1h, A1l, sw128_offset(i, c0, 128), Qg);
+            split_store2(A1h, A1l, sw128_offset(64 + i, c0, 128), Kg);
+            split_store2(B1h, B1l, sw128_offset(i, c0, 64), Kd);
+            const float2 a2v = f2_split(f2_mul(f2_make(bt[rr], bt[rr]), Kg));
+            const float2 klv = f2_split(f2_mul(Kd, gam2));
+            a2[0][e] = a2v.x;
+            a2[1][e] = a2v.y;
+            kl[0][e] = klv.x;
+            kl[1][e] = klv.y;
             if (i < L) {
               const size_t tok = size_t(t0 + i) * P.Hv + hv;
               if (out.Qs)
                 *reinterpret_cast<uint32_t*>(reinterpret_cast<__nv_bfloat16*>(out.Qs) + tok * K + c0) =
-                    pack_bf16x2(P.scale * Qg.x, P.scale * Qg.y);
-              if (out.G) *reinterpret_cast<float2*>(out.G + tok * K + c0) = G;
+                    f2_to_bf16x2(f2_mul(Qg, scale2));
+              if (out.G) *reinterpret_cast<float2*>(out.G + tok * K + c0) = f2_split(G2);
             }
           }
           const int col = kRowsPerThread * quarter + 8 * half;

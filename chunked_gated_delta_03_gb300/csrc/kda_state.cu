@@ -5,9 +5,11 @@
 //
 // Everything is computed transposed so that every MMA has M = 128 (the value
 // channel v, one TMEM lane per v) and all operands are K-major SWIZZLE_128B:
-//   [P^T | O^T] = S^T [W; Qs]^T     (M=128 v, N=128, K=K)   TMEM cols 128b .. 128b+127 (2 buffers)
-//   O^T += Delta^T Aqk^T            (M=128 v, N=64,  K=64)  TMEM cols 128b+64 ..
+//   P^T  = S^T W^T                  (M=128 v, N=64,  K=K)   TMEM cols 128b ..      (2 buffers)
+//   O^T  = S^T Qs^T                 (M=128 v, N=64,  K=K)   TMEM cols 128b+64 ..
 //   H^T  = Delta^T Kl               (M=128 v, N=K,   K=64)  TMEM cols 256 ..
+//   O^T += Delta^T Aqk^T            (M=128 v, N=64,  K=64)  TMEM cols 128b+64 ..
+// issued in that order, so that P and H, which gate the chunk chain, land first.
 // with Delta = U - W S (rows past the chunk's L valid rows forced to 0),
 // Qs = scale q e^G, Kl = k e^{G_last - G}, and the update
 //   S <- Diag(e^{G_last}) S + Kl^T Delta.
@@ -46,8 +48,8 @@ struct StateLayout {
   static constexpr uint32_t ringB = kStagesA * stageA_bytes;
   static constexpr uint32_t S = ringB + kStagesB * stageB_bytes;  // 128 x K, K-major SW128 (A operand S^T)
   static constexpr uint32_t D = S + 128 * K * 2;          // 128 x 64 (A operand Delta^T)
-  static constexpr uint32_t bars = D + 128 * 64 * 2;      // fullA[2], emptyA[2], fullB[3], emptyB[3], P, H, sready, dready
-  static constexpr uint32_t tmem_slot = bars + 14 * 8;
+  static constexpr uint32_t bars = D + 128 * 64 * 2;      // fullA[2], emptyA[2], fullB[3], emptyB[3], P, H, sready, dready, O
+  static constexpr uint32_t tmem_slot = bars + 16 * 8;
   static constexpr uint32_t abort_slot = tmem_slot + 4;
   static constexpr uint32_t total = abort_slot + 4;
   static constexpr uint32_t bytes = total + 1024;
@@ -99,6 +101,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
   uint64_t* bar_H = fullA + 11;
   uint64_t* sready = fullA + 12;
   uint64_t* dready = fullA + 13;
+  uint64_t* bar_O = fullA + 14;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + Lay::tmem_slot);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + Lay::abort_slot);
 
@@ -116,6 +119,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
     mbar_init(bar_H, 1);
     mbar_init(sready, 128);
     mbar_init(dready, 128);
+    mbar_init(bar_O, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -171,7 +175,6 @@ __global__ void __launch_bounds__(kStateThreads, 1)
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t id64 = idesc_bf16_f32(128, 64);
-      constexpr uint32_t id128 = idesc_bf16_f32(128, 128);
       constexpr uint32_t idK = idesc_bf16_f32(128, K);
       const uint32_t sS = smem_u32(sm + Lay::S), sD = smem_u32(sm + Lay::D);
       for (int c = 0; c < nch; ++c) {
@@ -181,13 +184,18 @@ __global__ void __launch_bounds__(kStateThreads, 1)
         wait_bar(&fullA[sa], (c / kStagesA) & 1, abort_flag, P.status);
         wait_bar(sready, c & 1, abort_flag, P.status);
         tc_fence_after();
-        umma_kloop(tmem + pcol, sS, 128, st + Lay::WQ, 128, K / 16, id128, 0);
+        // P^T = S^T W^T first (it gates the chain), then O^T = S^T Qs^T: the W
+        // rows are rows 0-63 and the Qs rows 64-127 of every 128-row atom.
+        umma_kloop(tmem + pcol, sS, 128, st + Lay::WQ, 128, K / 16, id64, 0);
         umma_commit(bar_P);
+        umma_kloop(tmem + ocol, sS, 128, st + Lay::WQ + 64 * 128, 128, K / 16, id64, 0);
         wait_bar(dready, c & 1, abort_flag, P.status);
         tc_fence_after();
-        umma_kloop(tmem + ocol, sD, 128, st + Lay::Aqk, 64, 4, id64, 1);
+        // H^T = Delta^T Kl first (it gates the next chunk), then O^T += Delta^T Aqk^T
         umma_kloop(tmem + 256, sD, 128, st + Lay::Kl, K, 4, idK, 0);
         umma_commit(bar_H);
+        umma_kloop(tmem + ocol, sD, 128, st + Lay::Aqk, 64, 4, id64, 1);
+        umma_commit(bar_O);
         umma_commit(&emptyA[sa]);
       }
     }
@@ -256,6 +264,8 @@ __global__ void __launch_bounds__(kStateThreads, 1)
       // O of this chunk sits in its own TMEM buffer; the next chunk writes the
       // other one, and the chunk after that waits for this thread's next
       // sready arrival, which comes after these loads.
+      wait_bar(bar_O, c & 1, abort_flag, P.status);
+      tc_fence_after();
       {
         uint32_t orow[64];
         tmem_ld_x64(tmem_addr(tmem + ocol, 32 * q4, 0), orow);

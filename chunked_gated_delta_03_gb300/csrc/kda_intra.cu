@@ -17,13 +17,15 @@
 //        A1_lo B1_hi^T (M=128, N=64; rows 0-63 Aqk/scale, rows 64-127 Akk/beta,
 //        ~FP32-accurate), then MMA2(j-1): W^T = (beta*Kg)^T Akk_inv^T and
 //        U^T = (beta*v)^T Akk_inv^T (M=128, N=64, K=64).
-//  epi   (warps 8-11, TMEM quadrants 0-3): W/U of item j-1 from TMEM to
-//        global; then D1(j): Aqk rows (quadrants 0,1) scaled and causally
-//        masked to global (fp32 export and the bf16 copy for the state pass),
-//        Akk rows (quadrants 2,3) beta-scaled and strictly masked into shared
-//        memory, where quadrants 2,3 invert (I + Akk) by forward substitution
-//        in FP32, one column of the inverse per thread, into the bf16 B2 tile
-//        of slot j%2 and the fp32 export.
+//  epi   (warps 8-11, TMEM quadrants 0-3): W/U of item j-1 from TMEM as
+//        bf16 staging tiles in its A2/A3 slot, stored by TMA; then D1(j): Aqk
+//        rows (quadrants 0,1) scaled and causally masked to global (fp32
+//        export and the bf16 copy for the state pass), Akk rows (quadrants
+//        2,3) beta-scaled and strictly masked into shared memory, where
+//        quadrants 2,3 invert (I + Akk) in FP32 by 16 x 16 blocks (forward
+//        substitution on the diagonal blocks, then three block diagonals of
+//        T = A X, X = -X_ii T) into the bf16 B2 tile of slot j%2 and the fp32
+//        export.
 //
 // TMEM: D1 double-buffered at columns 0 / 64; W^T, U^T double-buffered at
 // 128 / 256 (W) and +64 (U).  Shared memory: A1/B1 (single), A2/A3 and B2

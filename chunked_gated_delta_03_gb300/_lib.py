@@ -20,6 +20,8 @@ KDA_ERR_LAUNCH = -5
 KDA_ERR_WORKSPACE = -6
 KDA_ERR_BAD_SEQLENS = -16
 KDA_ERR_TIMEOUT = -17
+KDA_ERR_GATE_RANGE = -18
+KDA_MAX_CHUNK_LOG_DECAY = 60.0
 KDA_DTYPE_BF16 = 0
 KDA_DTYPE_FP32 = 1
 

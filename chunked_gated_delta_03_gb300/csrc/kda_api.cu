@@ -318,6 +318,8 @@ extern "C" const char* kda_status_string(int status) {
     case KDA_ERR_WORKSPACE: return "workspace smaller than kda_workspace_size()";
     case KDA_ERR_BAD_SEQLENS: return "cu_seqlens must start at 0, be non-decreasing and end at T";
     case KDA_ERR_TIMEOUT: return "a bounded wait inside a kernel ran out";
+    case KDA_ERR_GATE_RANGE:
+      return "a chunk's cumulative log-gate fell below -KDA_MAX_CHUNK_LOG_DECAY on some channel";
     default: return "unknown status";
   }
 }

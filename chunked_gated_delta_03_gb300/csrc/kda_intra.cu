@@ -240,6 +240,11 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
           glast.y += s.y;
         }
       }
+      // The decay factors e^{G_r - G_i} are formed as products of q e^{G} and
+      // k e^{-G}; both stay normal fp32 numbers only while the chunk's total
+      // log-decay on the channel is at most KDA_MAX_CHUNK_LOG_DECAY.
+      if (kact && quarter == 0 && fminf(glast.x, glast.y) < -KDA_MAX_CHUNK_LOG_DECAY)
+        set_status(P.status, KDA_ERR_GATE_RANGE);
       const float2 gam = make_float2(__expf(glast.x), __expf(glast.y));
       const size_t head_row = size_t(gc) * P.Hv + hv;
       if (kact && quarter == 0 && out.gamma) *reinterpret_cast<float2*>(out.gamma + head_row * K + c0) = gam;

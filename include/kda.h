@@ -60,6 +60,15 @@ extern "C" {
 
 typedef struct CUstream_st* kda_stream_t; /* a cudaStream_t; NULL = legacy default stream */
 
+/* Gate range.  The intra-chunk kernel forms each decay factor e^{G_r - G_i}
+ * (G the in-chunk cumulative log-gate) as the product of the operands
+ * q e^{G_r} and k e^{-G_i} on the tensor cores.  Both stay normal fp32 numbers
+ * while a chunk's total log-decay on every channel, -G at its last row, is at
+ * most this bound; a call whose input passes it sets the device status
+ * KDA_ERR_GATE_RANGE (read with kda_get_device_status) and its outputs are
+ * not valid.  Gates of the form -softplus(x)/16 decay a few units per chunk. */
+#define KDA_MAX_CHUNK_LOG_DECAY 60.0f
+
 enum kda_status {
   KDA_OK = 0,
   KDA_ERR_INVALID = -1,      /* null pointer, bad dimension or inconsistent argument */
@@ -69,7 +78,8 @@ enum kda_status {
   KDA_ERR_LAUNCH = -5,       /* a CUDA launch or tensor-map encode failed */
   KDA_ERR_WORKSPACE = -6,    /* workspace smaller than kda_workspace_size() */
   KDA_ERR_BAD_SEQLENS = -16, /* (device) cu_seqlens not 0..T and non-decreasing */
-  KDA_ERR_TIMEOUT = -17      /* (device) a bounded wait inside a kernel ran out */
+  KDA_ERR_TIMEOUT = -17,     /* (device) a bounded wait inside a kernel ran out */
+  KDA_ERR_GATE_RANGE = -18   /* (device) a chunk's cumulative log-gate fell below -KDA_MAX_CHUNK_LOG_DECAY */
 };
 
 enum kda_dtype { KDA_DTYPE_BF16 = 0, KDA_DTYPE_FP32 = 1 };

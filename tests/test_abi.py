@@ -51,7 +51,7 @@ def test_struct_layout_matches_header(tmp_path):
 
 
 def test_status_strings(lib):
-    for code in (0, -1, -2, -3, -4, -5, -6, -16, -17):
+    for code in (0, -1, -2, -3, -4, -5, -6, -16, -17, -18):
         s = _lib.status_string(code)
         assert s and s != "unknown status"
     assert _lib.status_string(12345) == "unknown status"

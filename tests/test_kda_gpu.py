@@ -202,6 +202,37 @@ def test_bad_cu_seqlens_sets_device_status():
     assert ops.device_status(ws) == _lib.KDA_OK
 
 
+def test_strong_gates_within_range_match_oracle():
+    # A per-step log-gate of -0.9 on every other channel: each full chunk then
+    # decays by 57.6 on those channels, just inside KDA_MAX_CHUNK_LOG_DECAY, so
+    # the operands q e^G and k e^-G span about 25 decades.
+    inp = make_inputs(WORKLOADS["tiny"], seed=43, T=200, initial_state=True)
+    g = inp["g"].clone()
+    g[..., ::2] = -0.9
+    inp["g"] = g
+    want = _oracle(inp)
+    out = _ours(_cuda(inp), inter=True)
+    _compare(inp, out, want, inter=True)
+
+
+def test_gates_past_the_range_set_device_status():
+    inp = _cuda(make_inputs(WORKLOADS["tiny"], seed=44, T=128))
+    inp["g"][:, 64:, 1, 5] = -1.0  # the second chunk decays by 64 on one channel of head 1
+    a, (B, T, Hq, Hv, K, V, N) = ops.make_args(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+                                               inp["scale"], None, None)
+    o = torch.zeros(B, T, Hv, V, dtype=torch.bfloat16, device="cuda")
+    a.o = o.data_ptr()
+    n = _lib.kda_workspace_size(a)
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    assert _lib.kda_chunk_fwd(a, ws.data_ptr(), n, stream) == _lib.KDA_OK
+    assert ops.device_status(ws) == _lib.KDA_ERR_GATE_RANGE
+    # back inside the range, a call on the same workspace clears the status
+    inp["g"][:, 64:, 1, 5] = -0.5
+    assert _lib.kda_chunk_fwd(a, ws.data_ptr(), n, stream) == _lib.KDA_OK
+    assert ops.device_status(ws) == _lib.KDA_OK
+
+
 def test_empty_inputs():
     inp = _cuda(make_inputs(WORKLOADS["tiny"], T=0, initial_state=True))
     o, final, _ = _ours(inp, inter=False)

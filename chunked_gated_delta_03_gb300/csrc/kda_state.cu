@@ -13,12 +13,13 @@
 // with Delta = U - W S (rows past the chunk's L valid rows forced to 0),
 // Qs = scale q e^G, Kl = k e^{G_last - G}, and the update
 //   S <- Diag(e^{G_last}) S + Kl^T Delta.
-// Epilogue thread v keeps column v of S (K fp32 values) in registers and
-// writes its bf16 copy as row v of the A operand S^T for the next chunk.
+// Two epilogue threads per value channel v (one per half of the columns)
+// keep column v of S in fp32 registers, K/2 values each, and write their
+// halves of row v of the A operand S^T for the next chunk.
 //
 // Warp roles: warp 0 issues TMA loads (and L2 prefetches one ring depth
-// ahead, so that the stage loads hit L2), warp 1 issues the MMAs, warps 2-5
-// (128 threads) run the epilogue.  Two rings: ring A (MMA operands [W; Qs],
+// ahead, so that the stage loads hit L2), warp 1 issues the MMAs, warps 2-9
+// (256 threads, two per TMEM lane quadrant) run the epilogue.  Two rings: ring A (MMA operands [W; Qs],
 // Aqk, Kl^T; 2 stages) is released by the MMAs' own completion, so the next
 // loads start mid-chunk; ring B (U and gamma, read by the epilogue; 3 stages)
 // is released by the epilogue.
@@ -28,7 +29,8 @@ namespace kda {
 
 namespace {
 
-constexpr int kStateThreads = 192;
+constexpr int kEpiThreads = 256;  // warps 2-9: two warps per TMEM lane quadrant
+constexpr int kStateThreads = 64 + kEpiThreads;
 constexpr int kStagesA = 2;
 constexpr int kStagesB = 3;
 
@@ -58,13 +60,14 @@ struct StateLayout {
   static_assert(bytes <= 227 * 1024, "shared memory budget");
 };
 
-template <int K>
-__device__ __forceinline__ void store_state_row(uint8_t* sS, int v, const float (&S)[K]) {
+// Columns k0 .. k0 + KH - 1 of row v of the A operand S^T (bf16, K-major SW128).
+template <int KH>
+__device__ __forceinline__ void store_state_part(uint8_t* sS, int v, int k0, const float (&S)[KH]) {
 #pragma unroll
-  for (int c = 0; c < K; c += 8) {
+  for (int c = 0; c < KH; c += 8) {
     const uint4 pk = make_uint4(pack_bf16x2(S[c], S[c + 1]), pack_bf16x2(S[c + 2], S[c + 3]),
                                 pack_bf16x2(S[c + 4], S[c + 5]), pack_bf16x2(S[c + 6], S[c + 7]));
-    *reinterpret_cast<uint4*>(sS + sw128_offset(v, c, 128)) = pk;
+    *reinterpret_cast<uint4*>(sS + sw128_offset(v, k0 + c, 128)) = pk;
   }
 }
 
@@ -112,12 +115,12 @@ __global__ void __launch_bounds__(kStateThreads, 1)
     }
     for (int s = 0; s < kStagesB; ++s) {
       mbar_init(&fullB[s], 1);
-      mbar_init(&emptyB[s], 4);
+      mbar_init(&emptyB[s], kEpiThreads / 32);
     }
     mbar_init(bar_P, 1);
     mbar_init(bar_H, 1);
-    mbar_init(sready, 128);
-    mbar_init(dready, 128);
+    mbar_init(sready, kEpiThreads);
+    mbar_init(dready, kEpiThreads);
     mbar_init(bar_O, 1);
     fence_mbar_init();
   }
@@ -203,16 +206,22 @@ __global__ void __launch_bounds__(kStateThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q4 = warp & 3;           // TMEM lane quadrant of this warp
-    const int v = 32 * q4 + lane;      // value channel owned by this thread
+    // Warps 2-9.  Warp w reads TMEM lane quadrant w % 4 (thread = value
+    // channel v); the two warps on a quadrant split the columns: half 0 takes
+    // tokens 0-31 of Delta and O and state channels 0 .. K/2 - 1, half 1 the rest.
+    constexpr int KH = K / 2;
+    const int q4 = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const int v = 32 * q4 + lane;
     const bool vv = v < V;
+    const int k0 = KH * half, r0 = 32 * half;
     uint8_t* sS = sm + Lay::S;
     uint8_t* sD = sm + Lay::D;
-    float S[K];
+    float S[KH];  // S[k0 + j][v]
     const size_t hbase = (size_t(n) * P.Hv + hv) * K;
 #pragma unroll
-    for (int k = 0; k < K; ++k) S[k] = (h0 && vv) ? h0[(hbase + k) * V + v] : 0.f;
-    store_state_row<K>(sS, v, S);
+    for (int j = 0; j < KH; ++j) S[j] = (h0 && vv) ? h0[(hbase + k0 + j) * V + v] : 0.f;
+    store_state_part<KH>(sS, v, k0, S);
     fence_proxy_async_smem();
     mbar_arrive(sready);
     for (int c = 0; c < nch; ++c) {
@@ -221,43 +230,46 @@ __global__ void __launch_bounds__(kStateThreads, 1)
       const int t0 = bos + c * kChunk;
       const int L = min(kChunk, len - c * kChunk);
       const uint32_t pcol = 128 * (c & 1), ocol = pcol + 64;
-      // Delta^T row v = U[:, v] - P^T row v, rows >= L zeroed
+      // Delta^T row v, tokens r0 .. r0 + 31: U[:, v] - P^T row v, rows >= L zeroed
       wait_bar(bar_P, c & 1, abort_flag, P.status);
       wait_bar(&fullB[sb], (c / kStagesB) & 1, abort_flag, P.status);
       tc_fence_after();
       const __nv_bfloat16* sU = reinterpret_cast<const __nv_bfloat16*>(st + Lay::U);
       {
-        uint32_t pr[64];
-        tmem_ld_x64(tmem_addr(tmem + pcol, 32 * q4, 0), pr);
+        uint32_t pr[32];
+        tmem_ld_x32(tmem_addr(tmem + pcol, 32 * q4, r0), pr);
 #pragma unroll
-        for (int j = 0; j < 64; j += 8) {
+        for (int j = 0; j < 32; j += 8) {
           float d[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
-            const int i = j + e;
+            const int i = r0 + j + e;
             const float u = vv ? __bfloat162float(sU[i * V + v]) : 0.f;
-            d[e] = (i < L) ? u - __uint_as_float(pr[i]) : 0.f;
+            d[e] = (i < L) ? u - __uint_as_float(pr[j + e]) : 0.f;
           }
           const uint4 pk = make_uint4(pack_bf16x2(d[0], d[1]), pack_bf16x2(d[2], d[3]),
                                       pack_bf16x2(d[4], d[5]), pack_bf16x2(d[6], d[7]));
-          *reinterpret_cast<uint4*>(sD + sw128_offset(v, j, 128)) = pk;
+          *reinterpret_cast<uint4*>(sD + sw128_offset(v, r0 + j, 128)) = pk;
         }
       }
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(dready);
-      // state update S <- gamma * S + H
+      // state update S <- gamma * S + H on channels k0 .. k0 + KH - 1
       wait_bar(bar_H, c & 1, abort_flag, P.status);
       tc_fence_after();
-      const float* sg = reinterpret_cast<const float*>(st + Lay::gam);
+      const float* sg = reinterpret_cast<const float*>(st + Lay::gam) + k0;
+      {
+        uint32_t hr[KH];
+        if constexpr (KH == 64) {
+          tmem_ld_x64(tmem_addr(tmem + 256 + k0, 32 * q4, 0), hr);
+        } else {
+          tmem_ld_x32(tmem_addr(tmem + 256 + k0, 32 * q4, 0), hr);
+        }
 #pragma unroll
-      for (int kb = 0; kb < K / 64; ++kb) {
-        uint32_t hr[64];
-        tmem_ld_x64(tmem_addr(tmem + 256 + 64 * kb, 32 * q4, 0), hr);
-#pragma unroll
-        for (int j = 0; j < 64; ++j) S[64 * kb + j] = fmaf(sg[64 * kb + j], S[64 * kb + j], __uint_as_float(hr[j]));
+        for (int j = 0; j < KH; ++j) S[j] = fmaf(sg[j], S[j], __uint_as_float(hr[j]));
       }
-      store_state_row<K>(sS, v, S);
+      store_state_part<KH>(sS, v, k0, S);
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(sready);
@@ -269,20 +281,20 @@ __global__ void __launch_bounds__(kStateThreads, 1)
       wait_bar(bar_O, c & 1, abort_flag, P.status);
       tc_fence_after();
       {
-        uint32_t orow[64];
-        tmem_ld_x64(tmem_addr(tmem + ocol, 32 * q4, 0), orow);
+        uint32_t orow[32];
+        tmem_ld_x32(tmem_addr(tmem + ocol, 32 * q4, r0), orow);
         if (vv) {
-          __nv_bfloat16* op = o + (size_t(t0) * P.Hv + hv) * V + v;
+          __nv_bfloat16* op = o + (size_t(t0 + r0) * P.Hv + hv) * V + v;
           const size_t ostride = size_t(P.Hv) * V;
 #pragma unroll
-          for (int r = 0; r < 64; ++r)
-            if (r < L) op[size_t(r) * ostride] = __float2bfloat16_rn(__uint_as_float(orow[r]));
+          for (int r = 0; r < 32; ++r)
+            if (r0 + r < L) op[size_t(r) * ostride] = __float2bfloat16_rn(__uint_as_float(orow[r]));
         }
       }
     }
     if (hT && vv) {
 #pragma unroll
-      for (int k = 0; k < K; ++k) hT[(hbase + k) * V + v] = S[k];
+      for (int j = 0; j < KH; ++j) hT[(hbase + k0 + j) * V + v] = S[j];
     }
   }
   tc_fence_before();

@@ -29,7 +29,8 @@ namespace kda {
 
 namespace {
 
-constexpr int kEpiThreads = 256;  // warps 2-9: two warps per TMEM lane quadrant
+constexpr int kEpiParts = 2;      // epilogue warps per TMEM lane quadrant (column split)
+constexpr int kEpiThreads = 128 * kEpiParts;
 constexpr int kStateThreads = 64 + kEpiThreads;
 constexpr int kStagesA = 2;
 constexpr int kStagesB = 3;
@@ -68,6 +69,19 @@ __device__ __forceinline__ void store_state_part(uint8_t* sS, int v, int k0, con
     const uint4 pk = make_uint4(pack_bf16x2(S[c], S[c + 1]), pack_bf16x2(S[c + 2], S[c + 3]),
                                 pack_bf16x2(S[c + 4], S[c + 5]), pack_bf16x2(S[c + 6], S[c + 7]));
     *reinterpret_cast<uint4*>(sS + sw128_offset(v, k0 + c, 128)) = pk;
+  }
+}
+
+// Warp-collective TMEM load of N (16, 32 or 64) consecutive columns.
+template <int N>
+__device__ __forceinline__ void tmem_ld_n(uint32_t taddr, uint32_t (&r)[N]) {
+  if constexpr (N == 64) {
+    tmem_ld_x64(taddr, r);
+  } else if constexpr (N == 32) {
+    tmem_ld_x32(taddr, r);
+  } else {
+    static_assert(N == 16, "16, 32 or 64 columns");
+    tmem_ld_x16(taddr, r);
   }
 }
 
@@ -209,12 +223,13 @@ __global__ void __launch_bounds__(kStateThreads, 1)
     // Warps 2-9.  Warp w reads TMEM lane quadrant w % 4 (thread = value
     // channel v); the two warps on a quadrant split the columns: half 0 takes
     // tokens 0-31 of Delta and O and state channels 0 .. K/2 - 1, half 1 the rest.
-    constexpr int KH = K / 2;
+    constexpr int KH = K / kEpiParts;   // state channels per thread
+    constexpr int RH = 64 / kEpiParts;  // tokens of Delta and O per thread
     const int q4 = warp & 3;
-    const int half = (warp - 2) >> 2;
+    const int half = (warp - 2) >> 2;   // column part 0 .. kEpiParts - 1
     const int v = 32 * q4 + lane;
     const bool vv = v < V;
-    const int k0 = KH * half, r0 = 32 * half;
+    const int k0 = KH * half, r0 = RH * half;
     uint8_t* sS = sm + Lay::S;
     uint8_t* sD = sm + Lay::D;
     float S[KH];  // S[k0 + j][v]
@@ -236,10 +251,10 @@ __global__ void __launch_bounds__(kStateThreads, 1)
       tc_fence_after();
       const __nv_bfloat16* sU = reinterpret_cast<const __nv_bfloat16*>(st + Lay::U);
       {
-        uint32_t pr[32];
-        tmem_ld_x32(tmem_addr(tmem + pcol, 32 * q4, r0), pr);
+        uint32_t pr[RH];
+        tmem_ld_n<RH>(tmem_addr(tmem + pcol, 32 * q4, r0), pr);
 #pragma unroll
-        for (int j = 0; j < 32; j += 8) {
+        for (int j = 0; j < RH; j += 8) {
           float d[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
@@ -261,11 +276,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
       const float* sg = reinterpret_cast<const float*>(st + Lay::gam) + k0;
       {
         uint32_t hr[KH];
-        if constexpr (KH == 64) {
-          tmem_ld_x64(tmem_addr(tmem + 256 + k0, 32 * q4, 0), hr);
-        } else {
-          tmem_ld_x32(tmem_addr(tmem + 256 + k0, 32 * q4, 0), hr);
-        }
+        tmem_ld_n<KH>(tmem_addr(tmem + 256 + k0, 32 * q4, 0), hr);
 #pragma unroll
         for (int j = 0; j < KH; ++j) S[j] = fmaf(sg[j], S[j], __uint_as_float(hr[j]));
       }
@@ -281,13 +292,13 @@ __global__ void __launch_bounds__(kStateThreads, 1)
       wait_bar(bar_O, c & 1, abort_flag, P.status);
       tc_fence_after();
       {
-        uint32_t orow[32];
-        tmem_ld_x32(tmem_addr(tmem + ocol, 32 * q4, r0), orow);
+        uint32_t orow[RH];
+        tmem_ld_n<RH>(tmem_addr(tmem + ocol, 32 * q4, r0), orow);
         if (vv) {
           __nv_bfloat16* op = o + (size_t(t0 + r0) * P.Hv + hv) * V + v;
           const size_t ostride = size_t(P.Hv) * V;
 #pragma unroll
-          for (int r = 0; r < 32; ++r)
+          for (int r = 0; r < RH; ++r)
             if (r0 + r < L) op[size_t(r) * ostride] = __float2bfloat16_rn(__uint_as_float(orow[r]));
         }
       }

@@ -122,6 +122,21 @@ def test_small_cases_match_oracle(case):
     _compare(inp, out, want, inter=True)
 
 
+@pytest.mark.parametrize("case", ["gva_init", "varlen"])
+def test_outputs_without_intermediates(case):
+    # W and U then live only in the workspace; o and the final state must
+    # match the oracle and, bit for bit, the call that exports them.
+    inp = make_inputs(WORKLOADS["tiny"], seed=200 + len(case), **SMALL_CASES[case])
+    want = _oracle(inp)
+    dev = _cuda(inp)
+    o, final, im = _ours(dev, inter=False)
+    assert im is None
+    _check("o", _np(o), want["o"], **TOL_STATE)
+    _check("final_state", _np(final), want["final_state"], **TOL_STATE)
+    o2, final2, _ = _ours(dev, inter=True)
+    assert torch.equal(o, o2) and torch.equal(final, final2)
+
+
 def test_intra_primitive_matches_oracle_and_full_path():
     inp = _cuda(make_inputs(WORKLOADS["tiny"], seed=7, **SMALL_CASES["varlen"]))
     intra = ops.chunk_kda_fwd_intra(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["scale"],

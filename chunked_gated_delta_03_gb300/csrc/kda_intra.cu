@@ -57,7 +57,8 @@ struct IntraLayout {
   static constexpr uint32_t sX = sAkk + 64 * kAkkLd * 4;    // fp32 64 x kAkkLd: Akk_inv, row-major
   static constexpr uint32_t sT = sX + 64 * kAkkLd * 4;       // fp32 3 x 16 x 16 block temporaries
   static constexpr uint32_t sPart = sT + 3 * 16 * 16 * 4;    // 2 x 4 x K floats
-  static constexpr uint32_t bars = sPart + 2 * 4 * K * 4;
+  static constexpr uint32_t sBeta = sPart + 2 * 4 * K * 4;  // 2 x 64 floats: beta of the item's rows
+  static constexpr uint32_t bars = sBeta + 2 * 64 * 4;
   static constexpr int kBars = 14;
   static constexpr uint32_t tmem_slot = bars + kBars * 8;
   static constexpr uint32_t abort_slot = tmem_slot + 4;
@@ -104,6 +105,13 @@ __device__ __forceinline__ void split_store2(uint8_t* hi_tile, uint8_t* lo_tile,
 __device__ __forceinline__ uint4 pack8(const float* f) {
   return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
                     pack_bf16x2(f[6], f[7]));
+}
+
+// beta[i] as fp32 from an fp32 or bf16 array, through the read-only path in
+// both cases (a plain load would be ordered after the kernel's own stores).
+__device__ __forceinline__ float load_beta(const void* beta, int fp32, size_t i) {
+  return fp32 ? __ldg(reinterpret_cast<const float*>(beta) + i)
+              : __bfloat162float(__ldg(reinterpret_cast<const __nv_bfloat16*>(beta) + i));
 }
 
 // Parity of the wait for the n-th completion (n >= 0) of a barrier.
@@ -162,21 +170,29 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
     const bool kact = c0 < K, vact = c0 < V;
     float* sPart = reinterpret_cast<float*>(sm + Lay::sPart);
     int j = 0;
-    for (long long item = blockIdx.x; item < n_items; item += gridDim.x) {
+    // Chunk lookups (dependent loads of the chunk table in varlen mode) run two
+    // items ahead, so that neither this item's loads nor the next item's L2
+    // prefetch wait for them.  Items are ordered by chunk and only the chunks
+    // past the last valid one are invalid, so the loop ends at the first
+    // invalid item.
+    auto lookup = [&](long long it) {
+      return it < n_items ? chunk_info(P, int(it / P.Hv)) : ChunkInfo{0, 0, 0, 0, false};
+    };
+    ChunkInfo ci = lookup(blockIdx.x);
+    ChunkInfo nci = lookup(blockIdx.x + gridDim.x);
+    for (long long item = blockIdx.x; item < n_items && ci.valid; item += gridDim.x) {
       const int hv = int(item % P.Hv);
       const int gc = int(item / P.Hv);
-      const ChunkInfo ci = chunk_info(P, gc);
-      if (!ci.valid) continue;
       const int hq = hv / grp;
       const int L = ci.L, t0 = ci.t0;
+      const long long nitem = item + gridDim.x;
+      const ChunkInfo nnci = lookup(nitem + gridDim.x);
       {
         // L2 prefetch of this thread's rows of the next item (one thread per 128-B line)
-        const long long nitem = item + gridDim.x;
-        if (nitem < n_items) {
+        if (nci.valid) {
           const int nhv = int(nitem % P.Hv);
-          const ChunkInfo nci = chunk_info(P, int(nitem / P.Hv));
           const int nhq = nhv / grp;
-          if (nci.valid) {
+          {
 #pragma unroll 1
             for (int rr = 0; rr < kRowsPerThread; ++rr) {
               const int i = kRowsPerThread * quarter + rr;
@@ -195,13 +211,11 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
       // ---- loads (all in flight together)
       float2 g2[kRowsPerThread];
       uint32_t q2[kRowsPerThread], k2[kRowsPerThread], v2[kRowsPerThread];
-      float bt[kRowsPerThread];
 #pragma unroll
       for (int rr = 0; rr < kRowsPerThread; ++rr) {
         const int i = kRowsPerThread * quarter + rr;
         g2[rr] = make_float2(0.f, 0.f);
         q2[rr] = k2[rr] = v2[rr] = 0u;
-        bt[rr] = 0.f;
         if (i < L) {
           const size_t tq = size_t(t0 + i) * P.Hq + hq, tv = size_t(t0 + i) * P.Hv + hv;
           if (kact) {
@@ -211,10 +225,15 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
           }
           if (vact)
             v2[rr] = __ldg(reinterpret_cast<const uint32_t*>(reinterpret_cast<const __nv_bfloat16*>(vp) + tv * V + c0));
-          bt[rr] = P.beta_fp32 ? __ldg(reinterpret_cast<const float*>(beta) + tv)
-                               : __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(beta)[tv]);
         }
       }
+      // ---- beta of the item's rows, once, as fp32 in shared memory (read by
+      // every channel pair after the barrier below; two buffers, because the
+      // next item's loads may start before slower threads finish this one)
+      float* bt = reinterpret_cast<float*>(sm + Lay::sBeta) + (j & 1) * 64 + kRowsPerThread * quarter;
+      if (tid < 64)
+        bt[tid - kRowsPerThread * quarter] =
+            tid < L ? load_beta(beta, P.beta_fp32, size_t(t0 + tid) * P.Hv + hv) : 0.f;
       // ---- cumsum offsets across row quarters
       float* part = sPart + (j & 1) * 4 * K;
       if (kact) {
@@ -227,6 +246,15 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         *reinterpret_cast<float2*>(part + quarter * K + c0) = s;
       }
       named_bar_sync(1, kPrepThreads);
+      float btv[kRowsPerThread];  // beta of this thread's rows
+#pragma unroll
+      for (int q = 0; q < kRowsPerThread / 4; ++q) {
+        const float4 b4 = reinterpret_cast<const float4*>(bt)[q];
+        btv[4 * q] = b4.x;
+        btv[4 * q + 1] = b4.y;
+        btv[4 * q + 2] = b4.z;
+        btv[4 * q + 3] = b4.w;
+      }
       float2 G = make_float2(0.f, 0.f), glast = make_float2(0.f, 0.f);
       if (kact) {
 #pragma unroll
@@ -283,7 +311,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
             split_store2(A1h, A1l, sw128_offset(i, c0, 128), Qg);
             split_store2(A1h, A1l, sw128_offset(64 + i, c0, 128), Kg);
             split_store2(B1h, B1l, sw128_offset(i, c0, 64), Kd);
-            const float2 a2v = f2_split(f2_mul(f2_make(bt[rr], bt[rr]), Kg));
+            const float2 a2v = f2_split(f2_mul(f2_make(btv[rr], btv[rr]), Kg));
             const float2 klv = f2_split(f2_mul(Kd, gam2));
             a2[0][e] = a2v.x;
             a2[1][e] = a2v.y;
@@ -315,8 +343,8 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
           for (int e = 0; e < 8; ++e) {
             const int rr = 8 * half + e;
             const float2 v = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v2[rr]));
-            a3[0][e] = bt[rr] * v.x;
-            a3[1][e] = bt[rr] * v.y;
+            a3[0][e] = btv[rr] * v.x;
+            a3[1][e] = btv[rr] * v.y;
           }
           const int col = kRowsPerThread * quarter + 8 * half;
           *reinterpret_cast<uint4*>(A3 + sw128_offset(c0, col, 128)) = pack8(a3[0]);
@@ -325,6 +353,8 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
       }
       fence_proxy_async_smem();
       mbar_arrive(&bar[kOpndFull]);
+      ci = nci;
+      nci = nnci;
       ++j;
     }
   } else {
@@ -461,11 +491,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         tmem_ld_x32(tmem_addr(d1, 32 * q4, 32), xb);
         tc_fence_before();
         mbar_arrive(&bar[kD1Empty + s]);
-        const float br = P.beta_fp32 ? (r < L ? __ldg(reinterpret_cast<const float*>(beta) + size_t(t0 + r) * P.Hv + hv)
-                                              : 0.f)
-                                     : (r < L ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(beta)
-                                                                     [size_t(t0 + r) * P.Hv + hv])
-                                              : 0.f);
+        const float br = r < L ? load_beta(beta, P.beta_fp32, size_t(t0 + r) * P.Hv + hv) : 0.f;
 #pragma unroll
         for (int c = 0; c < 64; c += 4) {
           float4 v4;

@@ -59,7 +59,7 @@ bool map_rows64(CUtensorMap* m, const void* base, long long rows, int box_rows) 
 }
 
 struct Layout {
-  size_t status = 0, nc = 4, idx = 0, off = 0, Qs = 0, Aqk_b = 0, KlT = 0, gamma = 0, W = 0, U = 0, total = 0;
+  size_t status = 0, nc = 4, idx = 0, off = 0, order = 0, Qs = 0, Aqk_b = 0, KlT = 0, gamma = 0, W = 0, U = 0, total = 0;
 };
 
 struct Shape {
@@ -111,6 +111,7 @@ Layout make_layout(const Shape& s, const KdaArgs* a, bool full) {
     L.off = take(size_t(s.N + 1) * 4);
   }
   if (full) {
+    if (s.varlen) L.order = take(size_t(s.N > 0 ? s.N : 1) * 4);
     L.Qs = take(size_t(s.BT) * s.Hv * s.K * 2);
     L.Aqk_b = take(size_t(s.BT) * s.Hv * 64 * 2);
     L.KlT = take(size_t(s.nc_max) * s.Hv * s.K * 64 * 2);
@@ -161,6 +162,7 @@ Problem make_problem(const Shape& s, const KdaArgs* a, uint8_t* ws, const Layout
     P.chunk_idx = reinterpret_cast<const int32_t*>(ws + L.idx);
     P.chunk_off = reinterpret_cast<const int32_t*>(ws + L.off);
     P.nc_dev = reinterpret_cast<const int32_t*>(ws + L.nc);
+    if (L.order) P.seq_order = reinterpret_cast<const int32_t*>(ws + L.order);
   }
   return P;
 }
@@ -187,6 +189,9 @@ int prologue(const KdaArgs* a, void* workspace, size_t ws_bytes, cudaStream_t st
     if (launch_chunk_index(a->cu_seqlens, s->N, s->T, kChunk, reinterpret_cast<int32_t*>(ws + L->idx),
                            reinterpret_cast<int32_t*>(ws + L->off), reinterpret_cast<int32_t*>(ws + L->nc),
                            reinterpret_cast<int32_t*>(ws + L->status), st) != cudaSuccess)
+      return KDA_ERR_LAUNCH;
+    if (full && launch_seq_order(a->cu_seqlens, s->N, s->T, kChunk, reinterpret_cast<int32_t*>(ws + L->order),
+                                 st) != cudaSuccess)
       return KDA_ERR_LAUNCH;
   }
   return KDA_OK;

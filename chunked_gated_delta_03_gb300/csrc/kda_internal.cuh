@@ -26,6 +26,7 @@ struct Problem {
   const int32_t* chunk_idx;  // varlen: [nc, 2] (sequence, chunk within sequence)
   const int32_t* chunk_off;  // varlen: [N + 1]
   const int32_t* nc_dev;     // varlen: number of chunks
+  const int32_t* seq_order;  // varlen state pass: sequences by chunk count, most first
   int32_t* status;           // device status word
 };
 
@@ -119,6 +120,7 @@ struct StateMaps {
 
 cudaError_t launch_chunk_index(const int32_t* cu, int N, int T, int chunk, int32_t* idx, int32_t* off,
                                int32_t* nc, int32_t* status, cudaStream_t s);
+cudaError_t launch_seq_order(const int32_t* cu, int N, int T, int chunk, int32_t* order, cudaStream_t s);
 cudaError_t launch_intra(const Problem& P, const IntraInputs& in, const IntraOut& out, const IntraStoreMaps& maps,
                          cudaStream_t s);
 cudaError_t launch_state(const Problem& P, const StateMaps& maps, const float* gamma, const float* h0,

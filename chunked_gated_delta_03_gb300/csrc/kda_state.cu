@@ -94,7 +94,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   const int hv = blockIdx.x % P.Hv;
-  const int n = blockIdx.x / P.Hv;
+  const int n = P.varlen ? P.seq_order[blockIdx.x / P.Hv] : blockIdx.x / P.Hv;  // longest chains first
   if (*reinterpret_cast<volatile int32_t*>(P.status) != 0) return;
   int bos, len, gc0;
   if (P.varlen) {

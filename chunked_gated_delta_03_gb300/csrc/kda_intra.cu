@@ -86,14 +86,6 @@ __device__ __forceinline__ float exp2f_fast(float x) {
   return y;
 }
 
-__device__ __forceinline__ void split_store(uint8_t* hi_tile, uint8_t* lo_tile, uint32_t off, float a, float b) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-  const float2 hf = __bfloat1622float2(h);
-  const __nv_bfloat162 l = __floats2bfloat162_rn(a - hf.x, b - hf.y);
-  *reinterpret_cast<__nv_bfloat162*>(hi_tile + off) = h;
-  *reinterpret_cast<__nv_bfloat162*>(lo_tile + off) = l;
-}
-
 // x = hi + lo with hi = bf16(x) and lo = bf16(x - hi), on a channel pair.
 __device__ __forceinline__ void split_store2(uint8_t* hi_tile, uint8_t* lo_tile, uint32_t off, f2 x) {
   const uint32_t h = f2_to_bf16x2(x);

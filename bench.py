@@ -185,6 +185,24 @@ def make_pool():
     return mp.get_context("spawn").Pool(cores), cores
 
 
+# ------------------------------------------------------------ ranks
+def max_over_ranks(ms, world, device):
+    """The slowest rank's time (every rank gets it); the rank's own time at world 1."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(ms, world, tokens_per_rank):
+    """Tokens per second of the whole job: every rank runs one replica of the
+    workload, and the job takes the slowest rank's time."""
+    return world * tokens_per_rank / (ms * 1e-3)
+
+
 # ------------------------------------------------------------------ main
 def main():
     ap = argparse.ArgumentParser()
@@ -310,11 +328,8 @@ def main():
     ms = t_start.elapsed_time(t_end) / args.steps
     intra_ms = statistics.mean(evs[i][0].elapsed_time(evs[i][1]) for i in range(args.steps))
     state_ms = statistics.mean(evs[i][1].elapsed_time(evs[i][2]) for i in range(args.steps))
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * B * T / (ms * 1e-3)
+    ms = max_over_ranks(ms, world, "cuda")
+    value = whole_job_rate(ms, world, B * T)
 
     # ---- end to end through the same C call, from/to pinned host memory.
     # Steps are pipelined the way a serving loop runs them: two device sets of

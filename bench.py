@@ -34,9 +34,11 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "KDA fwd ms/call & tokens/s, B=2 H=64 T=8192 K=V=128 bf16; % of roofline"
-# cuLA PR #131 (Performance table): complete public forward, B=2 H=64,
-# T=8192, FP32 beta, CuTeDSL: 0.8564 ms on SM100/SM103 (K, V not stated).
-PAGE_MS = {"mha_8k": 0.8564}
+# cuLA PR #131 (Performance table), CuTeDSL on SM100/SM103, K and V not
+# stated: the complete public forward at B=2 H=64 T=8192 with FP32 beta
+# (0.8564 ms) and T=1024 with BF16 beta (0.1320 ms); the grouped-value forward
+# at B=1 Hq=16 Hv=64 T=4096, BF16 (0.2379 ms).
+PAGE_MS = {"mha_8k": 0.8564, "mha_1k": 0.1320, "gva_4k": 0.2379}
 SMI_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -425,7 +427,8 @@ def main():
             "vs_baseline": (value / (B * T / (page * 1e-3))) if page else None,
             "dtype": "bf16", "data": "synthetic", "config": config,
             "kernels_ms": kern, "roofline": roof, "path_roofline": path, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": args.steps * (2 + (1 if host["cu_seqlens"] is not None else 0)),
+            # intra + state per step; varlen adds the chunk-table and sequence-order kernels
+            "gpu_launches": args.steps * (2 + (2 if host["cu_seqlens"] is not None else 0)),
             "clocks": clocks}
     print(json.dumps(line))
     if world > 1:

@@ -246,10 +246,14 @@ __global__ void __launch_bounds__(kStateThreads, 1)
       const int L = min(kChunk, len - c * kChunk);
       const uint32_t pcol = 128 * (c & 1), ocol = pcol + 64;
       // Delta^T row v, tokens r0 .. r0 + 31: U[:, v] - P^T row v, rows >= L zeroed
-      wait_bar(bar_P, c & 1, abort_flag, P.status);
+      // U[:, v] of this part's rows is read before P lands
       wait_bar(&fullB[sb], (c / kStagesB) & 1, abort_flag, P.status);
-      tc_fence_after();
       const __nv_bfloat16* sU = reinterpret_cast<const __nv_bfloat16*>(st + Lay::U);
+      float u[RH];
+#pragma unroll
+      for (int e = 0; e < RH; ++e) u[e] = vv ? __bfloat162float(sU[(r0 + e) * V + v]) : 0.f;
+      wait_bar(bar_P, c & 1, abort_flag, P.status);
+      tc_fence_after();
       {
         uint32_t pr[RH];
         tmem_ld_n<RH>(tmem_addr(tmem + pcol, 32 * q4, r0), pr);
@@ -259,8 +263,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const int i = r0 + j + e;
-            const float u = vv ? __bfloat162float(sU[i * V + v]) : 0.f;
-            d[e] = (i < L) ? u - __uint_as_float(pr[j + e]) : 0.f;
+            d[e] = (i < L) ? u[j + e] - __uint_as_float(pr[j + e]) : 0.f;
           }
           const uint4 pk = make_uint4(pack_bf16x2(d[0], d[1]), pack_bf16x2(d[2], d[3]),
                                       pack_bf16x2(d[4], d[5]), pack_bf16x2(d[6], d[7]));
@@ -270,15 +273,18 @@ __global__ void __launch_bounds__(kStateThreads, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(dready);
-      // state update S <- gamma * S + H on channels k0 .. k0 + KH - 1
+      // state update S <- gamma * S + H on channels k0 .. k0 + KH - 1: the
+      // decay is applied while the state MMA runs, H is added when it lands
+      const float* sg = reinterpret_cast<const float*>(st + Lay::gam) + k0;
+#pragma unroll
+      for (int j = 0; j < KH; ++j) S[j] *= sg[j];
       wait_bar(bar_H, c & 1, abort_flag, P.status);
       tc_fence_after();
-      const float* sg = reinterpret_cast<const float*>(st + Lay::gam) + k0;
       {
         uint32_t hr[KH];
         tmem_ld_n<KH>(tmem_addr(tmem + 256 + k0, 32 * q4, 0), hr);
 #pragma unroll
-        for (int j = 0; j < KH; ++j) S[j] = fmaf(sg[j], S[j], __uint_as_float(hr[j]));
+        for (int j = 0; j < KH; ++j) S[j] += __uint_as_float(hr[j]);
       }
       store_state_part<KH>(sS, v, k0, S);
       fence_proxy_async_smem();

@@ -110,8 +110,9 @@ struct IntraInputs {
   const void* beta;  // bf16 or fp32 [BT, Hv]
 };
 
-struct IntraStoreMaps {
-  CUtensorMap W, U;  // outputs, boxes of (D, 1, 64) rows, no swizzle
+struct IntraMaps {
+  CUtensorMap W, U;        // outputs, boxes of (D, 1, 64) rows, no swizzle
+  CUtensorMap q, k, v, g;  // inputs, same boxes: L2 prefetch of a whole chunk per tensor
 };
 
 struct StateMaps {
@@ -121,7 +122,7 @@ struct StateMaps {
 cudaError_t launch_chunk_index(const int32_t* cu, int N, int T, int chunk, int32_t* idx, int32_t* off,
                                int32_t* nc, int32_t* status, cudaStream_t s);
 cudaError_t launch_seq_order(const int32_t* cu, int N, int T, int chunk, int32_t* order, cudaStream_t s);
-cudaError_t launch_intra(const Problem& P, const IntraInputs& in, const IntraOut& out, const IntraStoreMaps& maps,
+cudaError_t launch_intra(const Problem& P, const IntraInputs& in, const IntraOut& out, const IntraMaps& maps,
                          cudaStream_t s);
 cudaError_t launch_state(const Problem& P, const StateMaps& maps, const float* gamma, const float* h0,
                          void* o, float* hT, cudaStream_t s);

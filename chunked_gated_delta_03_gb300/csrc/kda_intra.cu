@@ -113,7 +113,7 @@ template <int K, int V>
 __global__ void __launch_bounds__(kIntraThreads, 1)
     intra_kernel(const Problem P, const void* __restrict__ qp, const void* __restrict__ kp,
                  const void* __restrict__ vp, const float* __restrict__ gp, const void* __restrict__ beta,
-                 const IntraOut out, const __grid_constant__ IntraStoreMaps wu_maps) {
+                 const IntraOut out, const __grid_constant__ IntraMaps maps) {
   using Lay = IntraLayout<K, V>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -179,26 +179,14 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
       const int L = ci.L, t0 = ci.t0;
       const long long nitem = item + gridDim.x;
       const ChunkInfo nnci = lookup(nitem + gridDim.x);
-      {
-        // L2 prefetch of this thread's rows of the next item (one thread per 128-B line)
-        if (nci.valid) {
-          const int nhv = int(nitem % P.Hv);
-          const int nhq = nhv / grp;
-          {
-#pragma unroll 1
-            for (int rr = 0; rr < kRowsPerThread; ++rr) {
-              const int i = kRowsPerThread * quarter + rr;
-              if (i >= nci.L) break;
-              const size_t tq = size_t(nci.t0 + i) * P.Hq + nhq, tv = size_t(nci.t0 + i) * P.Hv + nhv;
-              if (kact && (p & 15) == 0) prefetch_l2(gp + tv * K + c0);
-              if (kact && (p & 31) == 0) {
-                prefetch_l2(reinterpret_cast<const __nv_bfloat16*>(qp) + tq * K + c0);
-                prefetch_l2(reinterpret_cast<const __nv_bfloat16*>(kp) + tq * K + c0);
-              }
-              if (vact && (p & 31) == 0) prefetch_l2(reinterpret_cast<const __nv_bfloat16*>(vp) + tv * V + c0);
-            }
-          }
-        }
+      if (tid == 0 && nci.valid) {
+        // L2 prefetch of the next item's chunk of q, k, v and g: one TMA
+        // prefetch per tensor (a box of 64 token rows of one head)
+        const int nhv = int(nitem % P.Hv), nhq = nhv / grp;
+        tma_prefetch_l2_3d(&maps.q, 0, nhq, nci.t0);
+        tma_prefetch_l2_3d(&maps.k, 0, nhq, nci.t0);
+        tma_prefetch_l2_3d(&maps.v, 0, nhv, nci.t0);
+        tma_prefetch_l2_3d(&maps.g, 0, nhv, nci.t0);
       }
       // ---- loads (all in flight together)
       float2 g2[kRowsPerThread];
@@ -423,8 +411,8 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
       }
       if (issuer) {
         if (full_chunk) {
-          tma_store_3d(&wu_maps.W, stage, 0, hv, t0);
-          tma_store_3d(&wu_maps.U, stage + 64 * K * 2, 0, hv, t0);
+          tma_store_3d(&maps.W, stage, 0, hv, t0);
+          tma_store_3d(&maps.U, stage + 64 * K * 2, 0, hv, t0);
           bulk_commit_group();
           bulk_wait_group_read0();
         }
@@ -595,7 +583,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
 }
 
 template <int K, int V>
-cudaError_t launch_intra_t(const Problem& P, const IntraInputs& in, const IntraOut& out, const IntraStoreMaps& maps,
+cudaError_t launch_intra_t(const Problem& P, const IntraInputs& in, const IntraOut& out, const IntraMaps& maps,
                            cudaStream_t s) {
   constexpr uint32_t smem = IntraLayout<K, V>::bytes;
   cudaError_t e = cudaFuncSetAttribute(intra_kernel<K, V>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -612,7 +600,7 @@ cudaError_t launch_intra_t(const Problem& P, const IntraInputs& in, const IntraO
 
 }  // namespace
 
-cudaError_t launch_intra(const Problem& P, const IntraInputs& in, const IntraOut& out, const IntraStoreMaps& maps,
+cudaError_t launch_intra(const Problem& P, const IntraInputs& in, const IntraOut& out, const IntraMaps& maps,
                          cudaStream_t s) {
   if (P.K == 128 && P.V == 128) return launch_intra_t<128, 128>(P, in, out, maps, s);
   if (P.K == 128 && P.V == 64) return launch_intra_t<128, 64>(P, in, out, maps, s);

@@ -248,6 +248,29 @@ def test_gates_past_the_range_set_device_status():
     assert ops.device_status(ws) == _lib.KDA_OK
 
 
+def test_zero_beta_is_pure_gated_decay():
+    # beta = 0: no delta updates.  Akk = 0, so Akk_inv is the identity and W, U
+    # vanish exactly; the state only decays, S_T = Diag(e^{sum_t g_t}) S0, and
+    # o_t = scale S0^T (q_t * e^{sum_{j<=t} g_j}) in closed form.
+    inp = make_inputs(WORKLOADS["tiny"], seed=47, T=200, initial_state=True)
+    inp["beta"] = torch.zeros_like(inp["beta"])
+    o, final, im = _ours(_cuda(inp), inter=True)
+    q = inp["q"].double().numpy()[0]              # [T, H, K]
+    g = inp["g"].double().numpy()[0]              # [T, H, K]
+    S0 = inp["initial_state"].double().numpy()[0]  # [H, K, V]
+    Gc = np.cumsum(g, axis=0)
+    want_final = np.exp(Gc[-1])[:, :, None] * S0
+    want_o = inp["scale"] * np.einsum("thk,hkv->thv", q * np.exp(Gc), S0)
+    _check("final_state", _np(final)[0], want_final, **TOL_STATE)
+    _check("o", _np(o)[0], want_o, **TOL_STATE)
+    T, H = q.shape[0], q.shape[1]
+    eye = np.zeros((T, H, 64))
+    for t in range(T):
+        eye[t, :, t % 64] = 1.0
+    assert np.array_equal(_np(im["Akk_inv"])[0], eye)
+    assert torch.count_nonzero(im["W"]) == 0 and torch.count_nonzero(im["U"]) == 0
+
+
 def test_empty_inputs():
     inp = _cuda(make_inputs(WORKLOADS["tiny"], T=0, initial_state=True))
     o, final, _ = _ours(inp, inter=False)

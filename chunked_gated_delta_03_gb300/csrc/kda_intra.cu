@@ -5,16 +5,21 @@
 // matrices, the FP32 inverse of (I + Akk), the W/U recompute), spread over
 // three warp groups so that consecutive items overlap:
 //
-//  prep  (warps 0-7, thread = channel pair x row quarter): load q, k, v, g,
-//        beta of item j straight from global memory (coalesced, all loads of a
-//        thread in flight together); inclusive cumsum G of g down the rows (the
-//        quarters exchange partial sums); gated operands Qg = q*e^G,
+//  prep  (warps 0-7, thread = channel pair x row quarter): one thread
+//        prefetches item j+1's q, k, v, g chunks into L2 (four TMA tensor
+//        prefetches); every thread loads its rows of q, k, v, g of item j
+//        straight from global memory (coalesced, all in flight together) and
+//        64 threads load the item's beta once into shared memory; inclusive
+//        cumsum G of g down the rows (the quarters exchange partial sums);
+//        a chunk whose log-decay on some channel passes
+//        KDA_MAX_CHUNK_LOG_DECAY sets KDA_ERR_GATE_RANGE; gated operands Qg = q*e^G,
 //        Kg = k*e^G, Kd = k*e^{-G}, split into bf16 hi + lo and written into
 //        K-major SWIZZLE_128B tiles A1 = [Qg; Kg] (128 x K), B1 = Kd (64 x K);
 //        (beta*Kg)^T and (beta*v)^T into the A2/A3 tiles of slot j%2; the
 //        state-pass operands Qs, Kl^T, gamma (and G) straight to global memory.
-//  mma   (lane 0 of warp 8, at the top of each item): MMA1(j): D1 = A1_hi B1_hi^T + A1_hi B1_lo^T +
-//        A1_lo B1_hi^T (M=128, N=64; rows 0-63 Aqk/scale, rows 64-127 Akk/beta,
+//  mma   (lane 0 of warp 8, at the top of each item): MMA1(j):
+//        D1 = A1_hi B1_hi^T + A1_hi B1_lo^T + A1_lo B1_hi^T
+//        (M=128, N=64; rows 0-63 Aqk/scale, rows 64-127 Akk/beta,
 //        ~FP32-accurate), then MMA2(j-1): W^T = (beta*Kg)^T Akk_inv^T and
 //        U^T = (beta*v)^T Akk_inv^T (M=128, N=64, K=64).
 //  epi   (warps 8-11, TMEM quadrants 0-3): W/U of item j-1 from TMEM as
@@ -29,7 +34,8 @@
 //
 // TMEM: D1 double-buffered at columns 0 / 64; W^T, U^T double-buffered at
 // 128 / 256 (W) and +64 (U).  Shared memory: A1/B1 (single), A2/A3 and B2
-// (two slots), the Akk tile, partial sums.  Every wait is bounded.
+// (two slots), the Akk tile and its inverse, partial sums, beta (two slots).
+// Every wait is bounded.
 #include "kda_internal.cuh"
 
 namespace kda {

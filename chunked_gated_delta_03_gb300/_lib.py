@@ -26,7 +26,7 @@ KDA_DTYPE_BF16 = 0
 KDA_DTYPE_FP32 = 1
 
 EXPORTS = ("kda_workspace_size", "kda_chunk_fwd", "kda_fwd_intra", "kda_prepare_chunk_indices",
-           "kda_get_device_status", "kda_status_string", "kda_chunk_fwd_static_scratch")
+           "kda_get_device_status", "kda_status_string", "kda_chunk_fwd_static_scratch", "kda_check_bounded_wait")
 KDA_STATIC_SCRATCH_BYTES = 64 << 20
 
 
@@ -94,6 +94,8 @@ def load():
     lib.kda_get_device_status.restype = ctypes.c_int
     lib.kda_chunk_fwd_static_scratch.argtypes = [P, ctypes.c_void_p, ctypes.c_void_p]
     lib.kda_chunk_fwd_static_scratch.restype = ctypes.c_int
+    lib.kda_check_bounded_wait.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+    lib.kda_check_bounded_wait.restype = ctypes.c_int
     lib.kda_status_string.argtypes = [ctypes.c_int]
     lib.kda_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -125,6 +127,11 @@ def kda_prepare_chunk_indices(cu_seqlens: int, N: int, T: int, chunk: int, chunk
                               chunk_offsets: int, num_chunks: int, status: int, stream: int) -> int:
     return int(load().kda_prepare_chunk_indices(cu_seqlens, N, T, chunk, chunk_indices, chunk_offsets,
                                                 num_chunks, status, stream))
+
+
+def kda_check_bounded_wait(device_status: int, stream: int) -> int:
+    """One warp waits on a barrier nothing arrives at; the bounded wait records KDA_ERR_TIMEOUT."""
+    return int(load().kda_check_bounded_wait(device_status, stream))
 
 
 def kda_get_device_status(workspace: int, stream: int) -> int:

@@ -316,6 +316,34 @@ extern "C" int kda_get_device_status(const void* workspace, kda_stream_t stream,
   return KDA_OK;
 }
 
+namespace kda {
+namespace {
+
+// One warp waits on a barrier that no thread arrives at: the bounded wait of
+// every kernel must give up, record the timeout and return.
+__global__ void bounded_wait_check_kernel(int32_t* status) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  wait_bar(&bar, 0, &abort_flag, status);
+}
+
+}  // namespace
+}  // namespace kda
+
+extern "C" int kda_check_bounded_wait(int32_t* device_status, kda_stream_t stream) {
+  if (!device_status) return KDA_ERR_INVALID;
+  const int rc = kda::check_arch();
+  if (rc) return rc;
+  kda::bounded_wait_check_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(device_status);
+  return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
+}
+
 extern "C" const char* kda_status_string(int status) {
   switch (status) {
     case KDA_OK: return "ok";

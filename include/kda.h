@@ -158,6 +158,16 @@ int kda_prepare_chunk_indices(const int32_t* cu_seqlens, int32_t N, int32_t T, i
  * or KDA_ERR_INVALID / KDA_ERR_LAUNCH when it could not read it. */
 int kda_get_device_status(const void* workspace, kda_stream_t stream, int32_t* status_out);
 
+/* Check of the bounded waits every kernel uses.  Launches one warp that waits
+ * on a shared-memory barrier nothing ever arrives at, through the same
+ * bounded wait as the kernels: after its limit (2 s) the wait gives up, the
+ * warp records KDA_ERR_TIMEOUT in *device_status (device int32 [1], first error
+ * kept) and returns, and the context stays usable.  Returns KDA_OK once the
+ * launch is enqueued on `stream`, or KDA_ERR_INVALID / KDA_ERR_ARCH /
+ * KDA_ERR_LAUNCH.  The pages have no counterpart; it exists so that the
+ * failure path can be exercised without faulting the GPU. */
+int kda_check_bounded_wait(int32_t* device_status, kda_stream_t stream);
+
 /* Bytes of the fixed device scratch behind kda_chunk_fwd_static_scratch. */
 #define KDA_STATIC_SCRATCH_BYTES ((size_t)64 << 20)
 

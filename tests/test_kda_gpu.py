@@ -271,6 +271,18 @@ def test_zero_beta_is_pure_gated_decay():
     assert torch.count_nonzero(im["W"]) == 0 and torch.count_nonzero(im["U"]) == 0
 
 
+def test_bounded_wait_gives_up_and_reports_timeout():
+    # a wait nothing satisfies ends after its limit with KDA_ERR_TIMEOUT in the
+    # status word, and the context stays usable for the next call
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    assert _lib.kda_check_bounded_wait(status.data_ptr(), stream) == _lib.KDA_OK
+    torch.cuda.synchronize()
+    assert int(status.item()) == _lib.KDA_ERR_TIMEOUT
+    inp = make_inputs(WORKLOADS["tiny"], seed=48)
+    _compare(inp, _ours(_cuda(inp), inter=True), _oracle(inp), inter=True)
+
+
 def test_empty_inputs():
     inp = _cuda(make_inputs(WORKLOADS["tiny"], T=0, initial_state=True))
     o, final, _ = _ours(inp, inter=False)

@@ -202,9 +202,7 @@ int run_intra(const Shape& s, const KdaArgs* a, const Problem& P, const IntraOut
   IntraMaps m;
   const auto bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const auto none = CU_TENSOR_MAP_SWIZZLE_NONE;
-  if (!map_tokens(&m.W, out.W, bf, 2, s.K, s.Hv, s.BT, s.K, none) ||
-      !map_tokens(&m.U, out.U, bf, 2, s.V, s.Hv, s.BT, s.V, none) ||
-      !map_tokens(&m.q, a->q, bf, 2, s.K, s.Hq, s.BT, s.K, none) ||
+  if (!map_tokens(&m.q, a->q, bf, 2, s.K, s.Hq, s.BT, s.K, none) ||
       !map_tokens(&m.k, a->k, bf, 2, s.K, s.Hq, s.BT, s.K, none) ||
       !map_tokens(&m.v, a->v, bf, 2, s.V, s.Hv, s.BT, s.V, none) ||
       !map_tokens(&m.g, a->g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, s.K, s.Hv, s.BT, s.K, none))

@@ -111,8 +111,7 @@ struct IntraInputs {
 };
 
 struct IntraMaps {
-  CUtensorMap W, U;        // outputs, boxes of (D, 1, 64) rows, no swizzle
-  CUtensorMap q, k, v, g;  // inputs, same boxes: L2 prefetch of a whole chunk per tensor
+  CUtensorMap q, k, v, g;  // inputs, boxes of (D, 1, 64) rows: L2 prefetch of a whole chunk per tensor
 };
 
 struct StateMaps {

@@ -5,37 +5,40 @@
 // matrices, the FP32 inverse of (I + Akk), the W/U recompute), spread over
 // three warp groups so that consecutive items overlap:
 //
-//  prep  (warps 0-7, thread = channel pair x row quarter): one thread
-//        prefetches item j+1's q, k, v, g chunks into L2 (four TMA tensor
-//        prefetches); every thread loads its rows of q, k, v, g of item j
+//  prep  (warps 0-7, thread = channel pair x row quarter): lane 0 of warps
+//        4-7 prefetch item j+1's q, k, v, g chunks into L2 (one TMA tensor
+//        prefetch each); every thread loads its rows of q, k, v, g of item j
 //        straight from global memory (coalesced, all in flight together) and
-//        64 threads load the item's beta once into shared memory; inclusive
-//        cumsum G of g down the rows (the quarters exchange partial sums);
-//        a chunk whose log-decay on some channel passes
-//        KDA_MAX_CHUNK_LOG_DECAY sets KDA_ERR_GATE_RANGE; gated operands Qg = q*e^G,
-//        Kg = k*e^G, Kd = k*e^{-G}, split into bf16 hi + lo and written into
-//        K-major SWIZZLE_128B tiles A1 = [Qg; Kg] (128 x K), B1 = Kd (64 x K);
-//        (beta*Kg)^T and (beta*v)^T into the A2/A3 tiles of slot j%2; the
-//        state-pass operands Qs, Kl^T, gamma (and G) straight to global memory.
-//  mma   (lane 0 of warp 8, at the top of each item): MMA1(j):
-//        D1 = A1_hi B1_hi^T + A1_hi B1_lo^T + A1_lo B1_hi^T
-//        (M=128, N=64; rows 0-63 Aqk/scale, rows 64-127 Akk/beta,
-//        ~FP32-accurate), then MMA2(j-1): W^T = (beta*Kg)^T Akk_inv^T and
-//        U^T = (beta*v)^T Akk_inv^T (M=128, N=64, K=64).
-//  epi   (warps 8-11, TMEM quadrants 0-3): W/U of item j-1 from TMEM as
-//        bf16 staging tiles in its A2/A3 slot, stored by TMA; then D1(j): Aqk
-//        rows (quadrants 0,1) scaled and causally masked to global (fp32
-//        export and the bf16 copy for the state pass), Akk rows (quadrants
-//        2,3) beta-scaled and strictly masked into shared memory, where
-//        quadrants 2,3 invert (I + Akk) in FP32 by 16 x 16 blocks (forward
-//        substitution on the diagonal blocks, then three block diagonals of
-//        T = A X, X = -X_ii T) into the bf16 B2 tile of slot j%2 and the fp32
-//        export.
+//        64 threads load the item's beta with them, into shared memory;
+//        inclusive cumsum G of g down the rows (the quarters exchange partial
+//        sums); a chunk whose log-decay on some channel passes
+//        KDA_MAX_CHUNK_LOG_DECAY sets KDA_ERR_GATE_RANGE; gated operands
+//        Qg = q*e^G, Kg = k*e^G, Kd = k*e^{-G}, split into bf16 hi + lo and
+//        written into K-major SWIZZLE_128B tiles A1 = [Qg; Kg] (128 x K, the
+//        Kg rows first for odd items), B1 = Kd (64 x K); (beta*Kg)^T and
+//        (beta*v)^T into the A2/A3 tiles of slot j%2; the state-pass operands
+//        Qs, Kl^T, gamma (and G) straight to global memory.
+//  epi   (warps 8-11, two pairs: warps 8, 9 read TMEM lanes 0-63, warps 10,
+//        11 lanes 64-127).  Item j is inverted by the pair whose lanes hold
+//        its Kg rows of D1 (pair 1 for even j, pair 0 for odd j): its leader
+//        issues MMA1(j),
+//          D1 = A1_hi B1_hi^T + A1_hi B1_lo^T + A1_lo B1_hi^T
+//        (M=128, N=64, ~FP32-accurate; the Qg rows give Aqk/scale, the Kg
+//        rows Akk/beta); the pair copies its Akk rows, beta-scaled and
+//        strictly masked, into shared memory as Akk^T, inverts (I + Akk) in
+//        FP32 by 16 x 16 blocks (forward substitution on the diagonal blocks,
+//        then three block diagonals of T = A X, X = -X_ii T), writes Akk_inv
+//        as the bf16 B2 tile of slot j%2 and the fp32 export, and its leader
+//        issues MMA2(j): W^T = (beta*Kg)^T Akk_inv^T, U^T = (beta*v)^T
+//        Akk_inv^T (M=128, N=64, K=64).  The other pair exports the Aqk rows
+//        (fp32, and the bf16 copy for the state pass).  Then both pairs store
+//        their channels of W/U of item j-1 from TMEM to global memory.  The
+//        inverses of consecutive items thus run on the two pairs at once.
 //
 // TMEM: D1 double-buffered at columns 0 / 64; W^T, U^T double-buffered at
 // 128 / 256 (W) and +64 (U).  Shared memory: A1/B1 (single), A2/A3 and B2
-// (two slots), the Akk tile and its inverse, partial sums, beta (two slots).
-// Every wait is bounded.
+// (two slots), per pair the Akk^T / Akk_inv tile and the diagonal blocks of
+// Akk_inv, partial sums, beta (two slots).  Every wait is bounded.
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -47,6 +50,8 @@ constexpr int kEpiWarp0 = kPrepWarps;     // warps 8..11; lane 0 of warp 8 also 
 constexpr int kIntraThreads = (kPrepWarps + 4) * 32;
 constexpr int kPrepThreads = kPrepWarps * 32;
 constexpr int kAkkLd = 68;  // fp32 row stride of the Akk tile (conflict-free float4 rows)
+constexpr int kXdLd = 20;   // fp32 row stride of a diagonal block of Akk_inv
+constexpr int kXdBlk = 16 * kXdLd + 16;  // fp32 stride between the diagonal blocks
 constexpr int kRowsPerThread = 16;
 
 template <int K, int V>
@@ -59,10 +64,13 @@ struct IntraLayout {
   static constexpr uint32_t A23_slot = 2 * 128 * 64 * 2;
   static constexpr uint32_t B2 = A23 + 2 * A23_slot;    // 2 slots x 64 x 64 bf16
   static constexpr uint32_t B2_slot = 64 * 64 * 2;
-  static constexpr uint32_t sAkk = B2 + 2 * B2_slot;    // fp32 64 x kAkkLd
-  static constexpr uint32_t sX = sAkk + 64 * kAkkLd * 4;    // fp32 64 x kAkkLd: Akk_inv, row-major
-  static constexpr uint32_t sT = sX + 64 * kAkkLd * 4;       // fp32 3 x 16 x 16 block temporaries
-  static constexpr uint32_t sPart = sT + 3 * 16 * 16 * 4;    // 2 x 4 x K floats
+  // per epilogue pair: M (fp32 64 x kAkkLd: Akk^T in the strict upper triangle,
+  // the off-diagonal blocks of Akk_inv below) and Xd (the four diagonal 16 x 16
+  // blocks of Akk_inv, dense)
+  static constexpr uint32_t sInv = B2 + 2 * B2_slot;
+  static constexpr uint32_t sInv_M = 64 * kAkkLd * 4;
+  static constexpr uint32_t sInv_pair = sInv_M + 4 * kXdBlk * 4;
+  static constexpr uint32_t sPart = sInv + 2 * sInv_pair;    // 2 x 4 x K floats
   static constexpr uint32_t sBeta = sPart + 2 * 4 * K * 4;  // 2 x 64 floats: beta of the item's rows
   static constexpr uint32_t bars = sBeta + 2 * 64 * 4;
   static constexpr int kBars = 14;
@@ -75,14 +83,14 @@ struct IntraLayout {
 
 // barrier indices
 enum {
-  kOpndFull = 0,   // prep -> mma: A1/B1/A2/A3 of item j written          (256 arrivals)
-  kA1Empty = 1,    // mma -> prep: MMA1 done reading A1/B1               (commit)
-  kA23Empty = 2,   // [2] epi -> prep: A2/A3 slot free (MMA2 and the W/U staging done; 1 arrival)
-  kD1Full = 4,     // [2] mma -> epi: D1 ready                           (commit)
-  kD1Empty = 6,    // [2] epi -> mma: D1 read                            (128 arrivals)
-  kB2Full = 8,     // [2] epi -> mma: B2 slot written                    (64 arrivals)
-  kD2Full = 10,    // [2] mma -> epi: W^T/U^T ready                      (commit)
-  kD2Empty = 12,   // [2] epi -> mma: W^T/U^T read                       (128 arrivals)
+  kOpndFull = 0,   // prep -> MMA1: A1/B1 of item j written              (256 arrivals)
+  kA1Empty = 1,    // MMA1 done reading A1/B1 -> prep                    (commit)
+  kA23Full = 2,    // [2] prep -> MMA2: A2/A3 slot written               (256 arrivals)
+  kA23Empty = 4,   // [2] MMA2 done reading the A2/A3 slot -> prep       (commit)
+  kD1Full = 6,     // [2] MMA1 -> epi: D1 ready                          (commit)
+  kD1Empty = 8,    // [2] epi -> MMA1: D1 read                           (128 arrivals)
+  kD2Full = 10,    // [2] MMA2 -> epi: W^T/U^T ready                     (commit)
+  kD2Empty = 12,   // [2] epi -> MMA2: W^T/U^T read                      (128 arrivals)
 };
 
 // 2^x by the MUFU ex2 instruction; e^x is taken as 2^(x log2 e).
@@ -129,18 +137,30 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + Lay::bars);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + Lay::tmem_slot);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + Lay::abort_slot);
-  const long long n_items = (long long)P.nc_max * P.Hv;
   const int grp = P.Hv / P.Hq;
+  // Work items (chunk gc, value head hv) in the order gc * Hv + hv, this CTA
+  // taking every gridDim.x-th: a cursor (x = hv, y = gc) stepped without division
+  const int step_h = int(gridDim.x % unsigned(P.Hv)), step_g = int(gridDim.x / unsigned(P.Hv));
+  auto advance = [&](int2 c) {
+    c.x += step_h;
+    c.y += step_g;
+    if (c.x >= P.Hv) {
+      c.x -= P.Hv;
+      ++c.y;
+    }
+    return c;
+  };
+  const int2 first = make_int2(int(blockIdx.x % unsigned(P.Hv)), int(blockIdx.x / unsigned(P.Hv)));
 
   if (tid == 0) {
     *abort_flag = 0;
     mbar_init(&bar[kOpndFull], kPrepThreads);
     mbar_init(&bar[kA1Empty], 1);
     for (int s = 0; s < 2; ++s) {
+      mbar_init(&bar[kA23Full + s], kPrepThreads);
       mbar_init(&bar[kA23Empty + s], 1);
       mbar_init(&bar[kD1Full + s], 1);
       mbar_init(&bar[kD1Empty + s], 128);
-      mbar_init(&bar[kB2Full + s], 64);
       mbar_init(&bar[kD2Full + s], 1);
       mbar_init(&bar[kD2Empty + s], 128);
     }
@@ -149,11 +169,6 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
   if (warp == kEpiWarp0) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
-  }
-  {
-    // blocks of Akk_inv above the diagonal are never written: zero them once
-    float* sX = reinterpret_cast<float*>(sm + Lay::sX);
-    for (int e = tid; e < 64 * kAkkLd; e += blockDim.x) sX[e] = 0.f;
   }
   tc_fence_before();
   __syncthreads();
@@ -173,26 +188,25 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
     // prefetch wait for them.  Items are ordered by chunk and only the chunks
     // past the last valid one are invalid, so the loop ends at the first
     // invalid item.
-    auto lookup = [&](long long it) {
-      return it < n_items ? chunk_info(P, int(it / P.Hv)) : ChunkInfo{0, 0, 0, 0, false};
+    auto lookup = [&](int2 c) {
+      return c.y < P.nc_max ? chunk_info(P, c.y) : ChunkInfo{0, 0, 0, 0, false};
     };
-    ChunkInfo ci = lookup(blockIdx.x);
-    ChunkInfo nci = lookup(blockIdx.x + gridDim.x);
-    for (long long item = blockIdx.x; item < n_items && ci.valid; item += gridDim.x) {
-      const int hv = int(item % P.Hv);
-      const int gc = int(item / P.Hv);
+    int2 cur = first, nxt = advance(first), nnx = advance(nxt);
+    ChunkInfo ci = lookup(cur);
+    ChunkInfo nci = lookup(nxt);
+    while (cur.y < P.nc_max && ci.valid) {
+      const int hv = cur.x;
+      const int gc = cur.y;
       const int hq = hv / grp;
       const int L = ci.L, t0 = ci.t0;
-      const long long nitem = item + gridDim.x;
-      const ChunkInfo nnci = lookup(nitem + gridDim.x);
-      if (tid == 0 && nci.valid) {
+      const ChunkInfo nnci = lookup(nnx);
+      if (lane == 0 && warp >= 4 && nci.valid) {
         // L2 prefetch of the next item's chunk of q, k, v and g: one TMA
-        // prefetch per tensor (a box of 64 token rows of one head)
-        const int nhv = int(nitem % P.Hv), nhq = nhv / grp;
-        tma_prefetch_l2_3d(&maps.q, 0, nhq, nci.t0);
-        tma_prefetch_l2_3d(&maps.k, 0, nhq, nci.t0);
-        tma_prefetch_l2_3d(&maps.v, 0, nhv, nci.t0);
-        tma_prefetch_l2_3d(&maps.g, 0, nhv, nci.t0);
+        // prefetch per tensor (a box of 64 token rows of one head), issued by
+        // lane 0 of warps 4-7 (not the warps that load beta)
+        const int nhv = nxt.x;
+        const CUtensorMap* m = warp == 4 ? &maps.q : warp == 5 ? &maps.k : warp == 6 ? &maps.v : &maps.g;
+        tma_prefetch_l2_3d(m, 0, warp < 6 ? nhv / grp : nhv, nci.t0);
       }
       // ---- loads (all in flight together)
       float2 g2[kRowsPerThread];
@@ -213,13 +227,12 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
             v2[rr] = __ldg(reinterpret_cast<const uint32_t*>(reinterpret_cast<const __nv_bfloat16*>(vp) + tv * V + c0));
         }
       }
-      // ---- beta of the item's rows, once, as fp32 in shared memory (read by
-      // every channel pair after the barrier below; two buffers, because the
-      // next item's loads may start before slower threads finish this one)
+      // ---- beta of the item's rows, loaded once by 64 threads with the rows
+      // above, as fp32 into shared memory (read by every channel pair after the
+      // barrier below; two buffers, because the next item's loads may start
+      // before slower threads finish this one)
       float* bt = reinterpret_cast<float*>(sm + Lay::sBeta) + (j & 1) * 64 + kRowsPerThread * quarter;
-      if (tid < 64)
-        bt[tid - kRowsPerThread * quarter] =
-            tid < L ? load_beta(beta, P.beta_fp32, size_t(t0 + tid) * P.Hv + hv) : 0.f;
+      const float bval = (tid < 64 && tid < L) ? load_beta(beta, P.beta_fp32, size_t(t0 + tid) * P.Hv + hv) : 0.f;
       // ---- cumsum offsets across row quarters
       float* part = sPart + (j & 1) * 4 * K;
       if (kact) {
@@ -231,6 +244,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         }
         *reinterpret_cast<float2*>(part + quarter * K + c0) = s;
       }
+      if (tid < 64) bt[tid - kRowsPerThread * quarter] = bval;
       named_bar_sync(1, kPrepThreads);
       float btv[kRowsPerThread];  // beta of this thread's rows
 #pragma unroll
@@ -267,6 +281,9 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
       if (j >= 2) wait_bar(&bar[kA23Empty + (j & 1)], par((j >> 1) - 1), abort_flag, P.status);
       uint8_t* A2 = sm + Lay::A23 + (j & 1) * Lay::A23_slot;
       uint8_t* A3 = A2 + 128 * 64 * 2;
+      // rows of Qg and Kg in A1: the D1 rows of Kg (Akk) land in the TMEM lanes
+      // of the epilogue pair that inverts this item
+      const int qrow = 64 * (j & 1), krow = 64 - qrow;
       // ---- gated operands
       if (kact) {
         f2 G2 = f2_make(G.x, G.y);
@@ -294,8 +311,8 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
             const f2 Qg = f2_mul(q, eG);
             const f2 Kg = f2_mul(k, eG);
             const f2 Kd = f2_mul(k, eN);
-            split_store2(A1h, A1l, sw128_offset(i, c0, 128), Qg);
-            split_store2(A1h, A1l, sw128_offset(64 + i, c0, 128), Kg);
+            split_store2(A1h, A1l, sw128_offset(qrow + i, c0, 128), Qg);
+            split_store2(A1h, A1l, sw128_offset(krow + i, c0, 128), Kg);
             split_store2(B1h, B1l, sw128_offset(i, c0, 64), Kd);
             const float2 a2v = f2_split(f2_mul(f2_make(btv[rr], btv[rr]), Kg));
             const float2 klv = f2_split(f2_mul(Kd, gam2));
@@ -339,18 +356,33 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
       }
       fence_proxy_async_smem();
       mbar_arrive(&bar[kOpndFull]);
+      mbar_arrive(&bar[kA23Full + (j & 1)]);
       ci = nci;
       nci = nnci;
+      cur = nxt;
+      nxt = nnx;
+      nnx = advance(nnx);
       ++j;
     }
+
   } else {
     // ================================================================ epi
-    const int q4 = warp & 3;        // TMEM lane quadrant
-    const int row = 32 * q4 + lane;  // TMEM lane of this thread
-    float* sAkk = reinterpret_cast<float*>(sm + Lay::sAkk);
-    const bool issuer = (warp == kEpiWarp0) && lane == 0;
+    // Two pairs of warps: pair 0 (warps 8, 9) reads TMEM lanes 0-63, pair 1
+    // (warps 10, 11) lanes 64-127.  For item j the pair whose lanes hold the
+    // Kg rows of D1 (pair 1 for even j, pair 0 for odd j) inverts (I + Akk)
+    // and issues MMA2(j); the other pair exports Aqk.  Then both store their
+    // channels of W/U of item j-1.  Consecutive inverses thus overlap.
+    const int q4 = warp & 3;                   // TMEM lane quadrant
+    const int pair = (warp - kEpiWarp0) >> 1;
+    const int r = lane + 32 * (q4 & 1);        // D1 row within the pair's 64 lanes
+    const uint32_t pair_bar = 2 + pair;        // named barrier of the pair's 64 threads
+    const bool leader = (warp & 1) == 0 && lane == 0;
+    float* M = reinterpret_cast<float*>(sm + Lay::sInv + pair * Lay::sInv_pair);
+    float* Xd = M + 64 * kAkkLd;
     constexpr uint32_t id = idesc_bf16_f32(128, 64);
-    // MMA1(jj): D1 = [Qg; Kg] Kd^T with the hi/lo split
+    // MMA1(jj), issued by the leader of the pair that inverts item jj, once
+    // every prep thread has written the item's A1/B1 tiles: D1 = [Qg; Kg] Kd^T
+    // with the hi/lo split (rows of Qg first for even items, of Kg for odd ones)
     auto mma1 = [&](int jj) {
       wait_bar(&bar[kOpndFull], par(jj), abort_flag, P.status);
       if (jj >= 2) wait_bar(&bar[kD1Empty + (jj & 1)], par((jj >> 1) - 1), abort_flag, P.status);
@@ -364,10 +396,10 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
       umma_commit(&bar[kD1Full + (jj & 1)]);
       umma_commit(&bar[kA1Empty]);
     };
-    // MMA2(jj): W^T = A2 B2^T, U^T = A3 B2^T
+    // MMA2(jj): W^T = A2 B2^T, U^T = A3 B2^T (leader of the inverting pair)
     auto mma2 = [&](int jj) {
       const int s = jj & 1;
-      wait_bar(&bar[kB2Full + s], par(jj >> 1), abort_flag, P.status);
+      wait_bar(&bar[kA23Full + s], par(jj >> 1), abort_flag, P.status);
       if (jj >= 2) wait_bar(&bar[kD2Empty + s], par((jj >> 1) - 1), abort_flag, P.status);
       tc_fence_after();
       const uint32_t a2 = smem_u32(sm + Lay::A23 + s * Lay::A23_slot);
@@ -376,75 +408,55 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
       umma_kloop(dW, a2, 128, b2, 64, 4, id, 0);
       umma_kloop(dW + 64, a2 + 128 * 64 * 2, 128, b2, 64, 4, id, 0);
       umma_commit(&bar[kD2Full + s]);
+      umma_commit(&bar[kA23Empty + s]);
     };
-    // W/U of a finished item: thread `row` is channel k (W) / v (U)
-    // W/U of a finished item jj (thread `row` = channel k of W / v of U).  Full
-    // chunks go through the item's A2/A3 slot (free once MMA2(jj) is done) as
-    // row-major staging tiles written out by TMA; the slot then returns to
-    // prep.  Partial chunks take plain stores.
+    // W/U of item jj from TMEM straight to global memory: thread = channel
+    // 32*q4 + lane, one bf16 per token (a warp writes 64 contiguous bytes).
     auto store_wu = [&](int jj, int t0, int L, int hv) {
       const int s = jj & 1;
       wait_bar(&bar[kD2Full + s], par(jj >> 1), abort_flag, P.status);
       tc_fence_after();
       const uint32_t dW = tmem + 128 + 128 * s;
-      uint8_t* stage = sm + Lay::A23 + s * Lay::A23_slot;
-      const bool full_chunk = L == kChunk;
+      const int ch = 32 * q4 + lane;
 #pragma unroll 1
       for (int part = 0; part < 2; ++part) {
         const int D = part == 0 ? K : V;
         uint32_t x[64];
         tmem_ld_x64(tmem_addr(dW + 64 * part, 32 * q4, 0), x);
         if (32 * q4 < D) {
-          if (full_chunk) {
-            __nv_bfloat16* st = reinterpret_cast<__nv_bfloat16*>(stage + part * 64 * K * 2) + row;
+          __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(part == 0 ? out.W : out.U) +
+                               (size_t(t0) * P.Hv + hv) * D + ch;
+          const size_t stride = size_t(P.Hv) * D;
 #pragma unroll
-            for (int r = 0; r < 64; ++r) st[r * D] = __float2bfloat16_rn(__uint_as_float(x[r]));
-          } else {
-            __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(part == 0 ? out.W : out.U) +
-                                 (size_t(t0) * P.Hv + hv) * D + row;
-            const size_t stride = size_t(P.Hv) * D;
-#pragma unroll
-            for (int r = 0; r < 64; ++r)
-              if (r < L) dst[size_t(r) * stride] = __float2bfloat16_rn(__uint_as_float(x[r]));
+          for (int t = 0; t < 64; ++t) {
+            if (t < L) *dst = __float2bfloat16_rn(__uint_as_float(x[t]));
+            dst += stride;
           }
         }
       }
       tc_fence_before();
       mbar_arrive(&bar[kD2Empty + s]);
-      if (full_chunk) {
-        fence_proxy_async_smem();
-        named_bar_sync(4, 128);
-      }
-      if (issuer) {
-        if (full_chunk) {
-          tma_store_3d(&maps.W, stage, 0, hv, t0);
-          tma_store_3d(&maps.U, stage + 64 * K * 2, 0, hv, t0);
-          bulk_commit_group();
-          bulk_wait_group_read0();
-        }
-        mbar_arrive(&bar[kA23Empty + s]);
-      }
     };
     int j = 0;
     int prev_t0 = 0, prev_L = 0, prev_hv = 0;
-    for (long long item = blockIdx.x; item < n_items; item += gridDim.x) {
-      const int hv = int(item % P.Hv);
-      const ChunkInfo ci = chunk_info(P, int(item / P.Hv));
+    for (int2 cur = first; cur.y < P.nc_max; cur = advance(cur)) {
+      const int hv = cur.x;
+      const ChunkInfo ci = chunk_info(P, cur.y);
       if (!ci.valid) continue;
       const int L = ci.L, t0 = ci.t0;
-      if (issuer) {
-        mma1(j);
-        if (j >= 1) mma2(j - 1);
-      }
-      __syncwarp();
-      if (j >= 1) store_wu(j - 1, prev_t0, prev_L, prev_hv);
       const int s = j & 1;
+      const bool inverts = s != pair;
+      // beta of row r (inverting pair), loaded before the waits below
+      const float br = (inverts && r < L) ? load_beta(beta, P.beta_fp32, size_t(t0 + r) * P.Hv + hv) : 0.f;
+      if (inverts) {
+        if (leader) mma1(j);
+        __syncwarp();
+      }
       wait_bar(&bar[kD1Full + s], par(j >> 1), abort_flag, P.status);
       tc_fence_after();
       const uint32_t d1 = tmem + 64 * s;
-      if (q4 < 2) {
-        // Aqk row r = row (lanes 0-63)
-        const int r = row;
+      if (!inverts) {
+        // Aqk row r
         const size_t tok = size_t(t0 + r) * P.Hv + hv;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -469,47 +481,38 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         tc_fence_before();
         mbar_arrive(&bar[kD1Empty + s]);
       } else {
-        // Akk row r (lanes 64-127) -> shared fp32, then invert
-        const int r = row - 64;
-        named_bar_sync(2, 64);  // previous inverse finished reading the Akk tile
+        // Akk row r, beta-scaled and strictly masked, into the strict upper
+        // triangle of M as Akk^T (M[c][r] = Akk[r][c], c < r).  The pair's
+        // previous inverse ended with a barrier after its last read of M.
         uint32_t xa[32], xb[32];
         tmem_ld_x32(tmem_addr(d1, 32 * q4, 0), xa);
         tmem_ld_x32(tmem_addr(d1, 32 * q4, 32), xb);
         tc_fence_before();
         mbar_arrive(&bar[kD1Empty + s]);
-        const float br = r < L ? load_beta(beta, P.beta_fp32, size_t(t0 + r) * P.Hv + hv) : 0.f;
 #pragma unroll
-        for (int c = 0; c < 64; c += 4) {
-          float4 v4;
-          const uint32_t* src = c < 32 ? xa : xb;
-          v4.x = (c + 0 < r) ? br * __uint_as_float(src[(c + 0) & 31]) : 0.f;
-          v4.y = (c + 1 < r) ? br * __uint_as_float(src[(c + 1) & 31]) : 0.f;
-          v4.z = (c + 2 < r) ? br * __uint_as_float(src[(c + 2) & 31]) : 0.f;
-          v4.w = (c + 3 < r) ? br * __uint_as_float(src[(c + 3) & 31]) : 0.f;
-          *reinterpret_cast<float4*>(sAkk + r * kAkkLd + c) = v4;
-        }
-        named_bar_sync(3, 64);
+        for (int c = 0; c < 64; ++c)
+          if (c < r) M[c * kAkkLd + r] = br * __uint_as_float(c < 32 ? xa[c] : xb[c - 32]);
+        named_bar_sync(pair_bar, 64);
         // X = (I + Akk)^{-1} by 16 x 16 blocks.  Diagonal blocks: forward
-        // substitution in registers, thread = (block d, column c).
-        float* sX = reinterpret_cast<float*>(sm + Lay::sX);
-        float* sT = reinterpret_cast<float*>(sm + Lay::sT);
+        // substitution in registers, thread = (block d, column c), into Xd.
         {
           const int d = r >> 4, c = r & 15, base = 16 * d;
           float x[16];
 #pragma unroll
           for (int rr = 0; rr < 16; ++rr) {
-            const float* arow = sAkk + (base + rr) * kAkkLd + base;
             float acc = 0.f;
 #pragma unroll
-            for (int i = 0; i < rr; ++i) acc = fmaf(arow[i], x[i], acc);
+            for (int i = 0; i < rr; ++i) acc = fmaf(M[(base + i) * kAkkLd + base + rr], x[i], acc);
             x[rr] = (rr == c ? 1.f : 0.f) - acc;
           }
+          float* xd = Xd + d * kXdBlk + c;
 #pragma unroll
-          for (int rr = 0; rr < 16; ++rr) sX[(base + rr) * kAkkLd + base + c] = x[rr];
+          for (int rr = 0; rr < 16; ++rr) xd[rr * kXdLd] = x[rr];
         }
-        named_bar_sync(3, 64);
+        named_bar_sync(pair_bar, 64);
         // Off-diagonal blocks, one block diagonal at a time:
-        //   T = Akk[16i + r, 16j : 16i] X[16j : 16i, 16j + cols],  X_ij = -X_ii T.
+        //   T = Akk[16i + r, 16j : 16i] X[16j : 16i, 16j + cols],  X_ij = -X_ii T,
+        // T held in the (i, j) block of M until X_ij replaces it.
         // Thread = (row r16, column quad cq) of each 16 x 16 block.
         const int r16 = r >> 2, cq = 4 * (r & 3);
 #pragma unroll 1
@@ -517,47 +520,72 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
 #pragma unroll 1
           for (int jb = 0; jb + lvl < 4; ++jb) {
             const int ib = jb + lvl;
-            const float* arow = sAkk + (16 * ib + r16) * kAkkLd;
+            const float* acol = M + 16 * ib + r16;  // acol[kk * kAkkLd] = Akk[16 ib + r16][kk]
+            const float* xdj = Xd + jb * kXdBlk + cq;
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
-            for (int kk = 16 * jb; kk < 16 * ib; ++kk) {
-              const float a = arow[kk];
-              const float4 xv = *reinterpret_cast<const float4*>(sX + kk * kAkkLd + 16 * jb + cq);
+            for (int kk = 0; kk < 16; ++kk) {
+              const float a = acol[(16 * jb + kk) * kAkkLd];
+              const float4 xv = *reinterpret_cast<const float4*>(xdj + kk * kXdLd);
               acc.x = fmaf(a, xv.x, acc.x);
               acc.y = fmaf(a, xv.y, acc.y);
               acc.z = fmaf(a, xv.z, acc.z);
               acc.w = fmaf(a, xv.w, acc.w);
             }
-            *reinterpret_cast<float4*>(sT + (jb * 16 + r16) * 16 + cq) = acc;
-          }
-          named_bar_sync(3, 64);
-#pragma unroll 1
-          for (int jb = 0; jb + lvl < 4; ++jb) {
-            const int ib = jb + lvl;
-            const float* xrow = sX + (16 * ib + r16) * kAkkLd + 16 * ib;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int kk = 0; kk < 16; ++kk) {
-              const float xv = xrow[kk];
-              const float4 t = *reinterpret_cast<const float4*>(sT + (jb * 16 + kk) * 16 + cq);
-              acc.x = fmaf(xv, t.x, acc.x);
-              acc.y = fmaf(xv, t.y, acc.y);
-              acc.z = fmaf(xv, t.z, acc.z);
-              acc.w = fmaf(xv, t.w, acc.w);
+#pragma unroll 4
+            for (int kk = 16 * jb + 16; kk < 16 * ib; ++kk) {
+              const float a = acol[kk * kAkkLd];
+              const float4 xv = *reinterpret_cast<const float4*>(M + kk * kAkkLd + 16 * jb + cq);
+              acc.x = fmaf(a, xv.x, acc.x);
+              acc.y = fmaf(a, xv.y, acc.y);
+              acc.z = fmaf(a, xv.z, acc.z);
+              acc.w = fmaf(a, xv.w, acc.w);
             }
-            *reinterpret_cast<float4*>(sX + (16 * ib + r16) * kAkkLd + 16 * jb + cq) =
-                make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+            *reinterpret_cast<float4*>(M + (16 * ib + r16) * kAkkLd + 16 * jb + cq) = acc;
           }
-          named_bar_sync(3, 64);
+          named_bar_sync(pair_bar, 64);
+          float4 xn[3];
+#pragma unroll
+          for (int jb = 0; jb < 3; ++jb) {
+            xn[jb] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (jb + lvl < 4) {
+              const int ib = jb + lvl;
+              const float* xrow = Xd + ib * kXdBlk + r16 * kXdLd;
+              float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+              for (int kk = 0; kk < 16; ++kk) {
+                const float xv = xrow[kk];
+                const float4 t = *reinterpret_cast<const float4*>(M + (16 * ib + kk) * kAkkLd + 16 * jb + cq);
+                acc.x = fmaf(xv, t.x, acc.x);
+                acc.y = fmaf(xv, t.y, acc.y);
+                acc.z = fmaf(xv, t.z, acc.z);
+                acc.w = fmaf(xv, t.w, acc.w);
+              }
+              xn[jb] = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+            }
+          }
+          named_bar_sync(pair_bar, 64);
+#pragma unroll
+          for (int jb = 0; jb < 3; ++jb)
+            if (jb + lvl < 4) *reinterpret_cast<float4*>(M + (16 * (jb + lvl) + r16) * kAkkLd + 16 * jb + cq) = xn[jb];
+          named_bar_sync(pair_bar, 64);
         }
-        // row r of X: bf16 B2 operand row and the fp32 export row
+        // row r of X: bf16 B2 operand row and the fp32 export row (blocks left
+        // of the diagonal from M, the diagonal block from Xd, zeros after it)
         uint8_t* B2 = sm + Lay::B2 + s * Lay::B2_slot;
-        const float* xr = sX + r * kAkkLd;
+        const int d = r >> 4;
+        const float* xoff = M + r * kAkkLd;
+        const float* xdia = Xd + d * kXdBlk + (r & 15) * kXdLd - 16 * d;
         float* inv_row = (out.Akk_inv && r < L) ? out.Akk_inv + (size_t(t0 + r) * P.Hv + hv) * 64 : nullptr;
 #pragma unroll
         for (int c8 = 0; c8 < 64; c8 += 8) {
-          const float4 u = *reinterpret_cast<const float4*>(xr + c8);
-          const float4 w = *reinterpret_cast<const float4*>(xr + c8 + 4);
+          const int blk = c8 >> 4;
+          float4 u = make_float4(0.f, 0.f, 0.f, 0.f), w = u;
+          if (blk <= d) {
+            const float* src = (blk < d ? xoff : xdia) + c8;
+            u = *reinterpret_cast<const float4*>(src);
+            w = *reinterpret_cast<const float4*>(src + 4);
+          }
           const float f[8] = {u.x, u.y, u.z, u.w, w.x, w.y, w.z, w.w};
           *reinterpret_cast<uint4*>(B2 + sw128_offset(r, c8, 64)) = pack8(f);
           if (inv_row) {
@@ -566,19 +594,17 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
           }
         }
         fence_proxy_async_smem();
-        mbar_arrive(&bar[kB2Full + s]);
+        named_bar_sync(pair_bar, 64);
+        if (leader) mma2(j);
+        __syncwarp();
       }
+      if (j >= 1) store_wu(j - 1, prev_t0, prev_L, prev_hv);
       prev_t0 = t0;
       prev_L = L;
       prev_hv = hv;
       ++j;
     }
-    if (j >= 1) {
-      if (issuer) mma2(j - 1);
-      __syncwarp();
-      store_wu(j - 1, prev_t0, prev_L, prev_hv);
-    }
-    if (issuer) bulk_wait_group0();
+    if (j >= 1) store_wu(j - 1, prev_t0, prev_L, prev_hv);
   }
   tc_fence_before();
   __syncthreads();

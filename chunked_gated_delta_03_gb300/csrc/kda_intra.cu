@@ -182,6 +182,14 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
     const int c0 = 2 * p;
     const bool kact = c0 < K, vact = c0 < V;
     float* sPart = reinterpret_cast<float*>(sm + Lay::sPart);
+    // Byte offset of this thread's channel pair in row r of a K-major
+    // SWIZZLE_128B tile: the atom, row, 16-byte chunk and in-chunk fields
+    // occupy disjoint bits, so the chunk's XOR with (r % 8) is one XOR with a
+    // per-row constant, applied to the row's base offset.
+    const uint32_t cbits = ((uint32_t(c0 & 63) >> 3) << 4) | (uint32_t(c0 & 7) << 1);
+    const uint32_t rows0 = uint32_t(kRowsPerThread * quarter) * 128u;
+    const uint32_t xA = uint32_t(c0 >> 6) * 128u * 128u + rows0 + cbits;  // A1, row 16*quarter
+    const uint32_t xB = uint32_t(c0 >> 6) * 64u * 128u + rows0 + cbits;   // B1, row 16*quarter
     int j = 0;
     // Chunk lookups (dependent loads of the chunk table in varlen mode) run two
     // items ahead, so that neither this item's loads nor the next item's L2
@@ -294,6 +302,11 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         uint8_t* A1l = sm + Lay::A1_lo;
         uint8_t* B1h = sm + Lay::B1_hi;
         uint8_t* B1l = sm + Lay::B1_lo;
+        const uint32_t xq = xA + uint32_t(qrow) * 128u, xk = xA + uint32_t(krow) * 128u;
+        __nv_bfloat16* qs_row = out.Qs ? reinterpret_cast<__nv_bfloat16*>(out.Qs) +
+                                             (size_t(t0 + kRowsPerThread * quarter) * P.Hv + hv) * K + c0
+                                       : nullptr;
+        const size_t qs_stride = size_t(P.Hv) * K;
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           float a2[2][8], kl[2][8];
@@ -311,10 +324,12 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
             const f2 Qg = f2_mul(q, eG);
             const f2 Kg = f2_mul(k, eG);
             const f2 Kd = f2_mul(k, eN);
-            split_store2(A1h, A1l, sw128_offset(qrow + i, c0, 128), Qg);
-            split_store2(A1h, A1l, sw128_offset(krow + i, c0, 128), Kg);
-            split_store2(B1h, B1l, sw128_offset(i, c0, 64), Kd);
-            const float2 a2v = f2_split(f2_mul(f2_make(btv[rr], btv[rr]), Kg));
+            const uint32_t swr = uint32_t(rr & 7) << 4, rowr = uint32_t(rr) * 128u;
+            split_store2(A1h, A1l, (xq ^ swr) + rowr, Qg);
+            split_store2(A1h, A1l, (xk ^ swr) + rowr, Kg);
+            split_store2(B1h, B1l, (xB ^ swr) + rowr, Kd);
+            const float2 kgv = f2_split(Kg);
+            const float2 a2v = make_float2(btv[rr] * kgv.x, btv[rr] * kgv.y);
             const float2 klv = f2_split(f2_mul(Kd, gam2));
             a2[0][e] = a2v.x;
             a2[1][e] = a2v.y;
@@ -322,9 +337,8 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
             kl[1][e] = klv.y;
             if (i < L) {
               const size_t tok = size_t(t0 + i) * P.Hv + hv;
-              if (out.Qs)
-                *reinterpret_cast<uint32_t*>(reinterpret_cast<__nv_bfloat16*>(out.Qs) + tok * K + c0) =
-                    f2_to_bf16x2(f2_mul(Qg, scale2));
+              if (qs_row)
+                *reinterpret_cast<uint32_t*>(qs_row + size_t(rr) * qs_stride) = f2_to_bf16x2(f2_mul(Qg, scale2));
               if (out.G) *reinterpret_cast<float2*>(out.G + tok * K + c0) = f2_split(G2);
             }
           }
@@ -387,12 +401,19 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
       wait_bar(&bar[kOpndFull], par(jj), abort_flag, P.status);
       if (jj >= 2) wait_bar(&bar[kD1Empty + (jj & 1)], par((jj >> 1) - 1), abort_flag, P.status);
       tc_fence_after();
-      const uint32_t a_hi = smem_u32(sm + Lay::A1_hi), a_lo = smem_u32(sm + Lay::A1_lo);
-      const uint32_t b_hi = smem_u32(sm + Lay::B1_hi), b_lo = smem_u32(sm + Lay::B1_lo);
+      const uint64_t a_hi = sdesc_kmajor_sw128(smem_u32(sm + Lay::A1_hi));
+      const uint64_t a_lo = sdesc_kmajor_sw128(smem_u32(sm + Lay::A1_lo));
+      const uint64_t b_hi = sdesc_kmajor_sw128(smem_u32(sm + Lay::B1_hi));
+      const uint64_t b_lo = sdesc_kmajor_sw128(smem_u32(sm + Lay::B1_lo));
       const uint32_t d1 = tmem + 64 * (jj & 1);
-      umma_kloop(d1, a_hi, 128, b_hi, 64, K / 16, id, 0);
-      umma_kloop(d1, a_hi, 128, b_lo, 64, K / 16, id, 1);
-      umma_kloop(d1, a_lo, 128, b_hi, 64, K / 16, id, 1);
+      // atoms of 64 channels: 128 rows of A1 (1024 descriptor units apart), 64
+      // rows of B1 (512 apart)
+#pragma unroll
+      for (int at = 0; at < K / 64; ++at) umma_atom4(d1, a_hi + at * 1024, b_hi + at * 512, id, at > 0);
+#pragma unroll
+      for (int at = 0; at < K / 64; ++at) umma_atom4(d1, a_hi + at * 1024, b_lo + at * 512, id, 1);
+#pragma unroll
+      for (int at = 0; at < K / 64; ++at) umma_atom4(d1, a_lo + at * 1024, b_hi + at * 512, id, 1);
       umma_commit(&bar[kD1Full + (jj & 1)]);
       umma_commit(&bar[kA1Empty]);
     };
@@ -402,11 +423,11 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
       wait_bar(&bar[kA23Full + s], par(jj >> 1), abort_flag, P.status);
       if (jj >= 2) wait_bar(&bar[kD2Empty + s], par((jj >> 1) - 1), abort_flag, P.status);
       tc_fence_after();
-      const uint32_t a2 = smem_u32(sm + Lay::A23 + s * Lay::A23_slot);
-      const uint32_t b2 = smem_u32(sm + Lay::B2 + s * Lay::B2_slot);
+      const uint64_t a2 = sdesc_kmajor_sw128(smem_u32(sm + Lay::A23 + s * Lay::A23_slot));
+      const uint64_t b2 = sdesc_kmajor_sw128(smem_u32(sm + Lay::B2 + s * Lay::B2_slot));
       const uint32_t dW = tmem + 128 + 128 * s;
-      umma_kloop(dW, a2, 128, b2, 64, 4, id, 0);
-      umma_kloop(dW + 64, a2 + 128 * 64 * 2, 128, b2, 64, 4, id, 0);
+      umma_atom4(dW, a2, b2, id, 0);
+      umma_atom4(dW + 64, a2 + (128 * 64 * 2) / 16, b2, id, 0);
       umma_commit(&bar[kD2Full + s]);
       umma_commit(&bar[kA23Empty + s]);
     };

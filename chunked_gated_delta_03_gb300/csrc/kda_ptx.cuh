@@ -212,6 +212,24 @@ __device__ __forceinline__ void umma_kloop(uint32_t d_tmem, uint32_t a_base, uin
   }
 }
 
+// Four MMAs of K = 16 over one 128-byte swizzle atom (K = 64), issued from
+// one asm block.  The descriptors' address field counts 16-byte units: a K
+// step of 16 bf16 (32 bytes) adds 2, and the next atom of an operand with
+// `rows` rows starts rows * 8 further on.  Only the first MMA takes the
+// caller's accumulate flag; the other three accumulate.
+__device__ __forceinline__ void umma_atom4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 q, %11, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %6, %3, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %8, %3, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %9, %10, %3, q;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "l"(a_desc + 2), "l"(b_desc + 2), "l"(a_desc + 4),
+      "l"(b_desc + 4), "l"(a_desc + 6), "l"(b_desc + 6), "r"(1u)
+      : "memory");
+}
+
 // Warp-collective TMEM load: lane i of the warp reads TMEM lane (taddr.lane + i),
 // 16 consecutive 32-bit columns starting at taddr.col, and waits for completion
 // inside the same asm block so no use of the registers can be hoisted above it.

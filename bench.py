@@ -82,7 +82,7 @@ def algorithmic_bytes(w, N):
 # SHA-1 of the sources the kernel was built from: once those change, the
 # number no longer describes the kernel and is not reported.
 MEASURED_TRAFFIC = {
-    ("mha_8k", "intra"): (1351188480 + 1700321792, "95f5e225514f022b0d11b93458f8c3ee6ae960f5"),
+    ("mha_8k", "intra"): (1351576576 + 1700227072, "39199a6e61afa9e66c6b79357fa0182e8bbeddc6"),
 }
 KERNEL_SOURCES = {"intra": ("kda_intra.cu", "kda_internal.cuh", "kda_ptx.cuh"),
                   "state": ("kda_state.cu", "kda_internal.cuh", "kda_ptx.cuh")}

@@ -205,7 +205,8 @@ int run_intra(const Shape& s, const KdaArgs* a, const Problem& P, const IntraOut
   if (!map_tokens(&m.q, a->q, bf, 2, s.K, s.Hq, s.BT, s.K, none) ||
       !map_tokens(&m.k, a->k, bf, 2, s.K, s.Hq, s.BT, s.K, none) ||
       !map_tokens(&m.v, a->v, bf, 2, s.V, s.Hv, s.BT, s.V, none) ||
-      !map_tokens(&m.g, a->g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, s.K, s.Hv, s.BT, s.K, none))
+      !map_tokens(&m.g, a->g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, s.K, s.Hv, s.BT, s.K, none) ||
+      !map_tokens(&m.v_sw, a->v, bf, 2, s.V, s.Hv, s.BT, 64, CU_TENSOR_MAP_SWIZZLE_128B))
     return KDA_ERR_LAUNCH;
   return launch_intra(P, in, out, m, st) == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
 }

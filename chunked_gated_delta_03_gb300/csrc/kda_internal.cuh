@@ -112,6 +112,7 @@ struct IntraInputs {
 
 struct IntraMaps {
   CUtensorMap q, k, v, g;  // inputs, boxes of (D, 1, 64) rows: L2 prefetch of a whole chunk per tensor
+  CUtensorMap v_sw;        // v, SWIZZLE_128B boxes of (64, 1, 64): the W/U MMA's A operand, MN-major
 };
 
 struct StateMaps {

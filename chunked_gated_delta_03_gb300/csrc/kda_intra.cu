@@ -7,17 +7,19 @@
 //
 //  prep  (warps 0-7, thread = channel pair x row quarter): lane 0 of warps
 //        4-7 prefetch item j+1's q, k, v, g chunks into L2 (one TMA tensor
-//        prefetch each); every thread loads its rows of q, k, v, g of item j
-//        straight from global memory (coalesced, all in flight together) and
-//        64 threads load the item's beta with them, into shared memory;
+//        prefetch each); every thread loads its rows of q, k, g of item j
+//        straight from global memory (coalesced, all in flight together);
 //        inclusive cumsum G of g down the rows (the quarters exchange partial
 //        sums); a chunk whose log-decay on some channel passes
 //        KDA_MAX_CHUNK_LOG_DECAY sets KDA_ERR_GATE_RANGE; gated operands
 //        Qg = q*e^G, Kg = k*e^G, Kd = k*e^{-G}, split into bf16 hi + lo and
 //        written into K-major SWIZZLE_128B tiles A1 = [Qg; Kg] (128 x K, the
-//        Kg rows first for odd items), B1 = Kd (64 x K); (beta*Kg)^T and
-//        (beta*v)^T into the A2/A3 tiles of slot j%2; the state-pass operands
-//        Qs, Kl^T, gamma (and G) straight to global memory.
+//        Kg rows first for odd items), B1 = Kd (64 x K); the state-pass
+//        operands Qs, Kl^T, gamma (and G) straight to global memory.  Then,
+//        once MMA2 of item j-2 has freed slot j%2, the bf16 Kg rows go into
+//        its A2 tile and one thread starts the TMA copy of the item's v chunk
+//        into its A3 tile (both token rows, MN-major for MMA2); a tail item
+//        clears the v rows past its last token once the copy has landed.
 //  epi   (warps 8-11, two pairs: warps 8, 9 read TMEM lanes 0-63, warps 10,
 //        11 lanes 64-127).  Item j is inverted by the pair whose lanes hold
 //        its Kg rows of D1 (pair 1 for even j, pair 0 for odd j): its leader
@@ -27,18 +29,18 @@
 //        rows Akk/beta); the pair copies its Akk rows, beta-scaled and
 //        strictly masked, into shared memory as Akk^T, inverts (I + Akk) in
 //        FP32 by 16 x 16 blocks (forward substitution on the diagonal blocks,
-//        then three block diagonals of T = A X, X = -X_ii T), writes Akk_inv
-//        as the bf16 B2 tile of slot j%2 and the fp32 export, and its leader
-//        issues MMA2(j): W^T = (beta*Kg)^T Akk_inv^T, U^T = (beta*v)^T
-//        Akk_inv^T (M=128, N=64, K=64).  The other pair exports the Aqk rows
+//        then three block diagonals of T = A X, X = -X_ii T), writes the fp32
+//        Akk_inv export and B2 = Akk_inv diag(beta) as the bf16 tile of slot
+//        j%2, and its leader issues MMA2(j): W^T = Kg^T B2^T, U^T = v^T B2^T
+//        (M=128, N=64, K=64, A MN-major).  The other pair exports the Aqk rows
 //        (fp32, and the bf16 copy for the state pass).  Then both pairs store
 //        their channels of W/U of item j-1 from TMEM to global memory.  The
 //        inverses of consecutive items thus run on the two pairs at once.
 //
 // TMEM: D1 double-buffered at columns 0 / 64; W^T, U^T double-buffered at
 // 128 / 256 (W) and +64 (U).  Shared memory: A1/B1 (single), A2/A3 and B2
-// (two slots), per pair the Akk^T / Akk_inv tile and the diagonal blocks of
-// Akk_inv, partial sums, beta (two slots).  Every wait is bounded.
+// (two slots), per pair the Akk^T / Akk_inv tile, the diagonal blocks of
+// Akk_inv and the item's beta, partial sums.  Every wait is bounded.
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -60,8 +62,11 @@ struct IntraLayout {
   static constexpr uint32_t A1_lo = A1_hi + 128 * K * 2;
   static constexpr uint32_t B1_hi = A1_lo + 128 * K * 2;
   static constexpr uint32_t B1_lo = B1_hi + 64 * K * 2;
-  static constexpr uint32_t A23 = B1_lo + 64 * K * 2;   // 2 slots x [A2 | A3], each 128 x 64
-  static constexpr uint32_t A23_slot = 2 * 128 * 64 * 2;
+  // 2 slots x [A2 | A3]: Kg (hi part) and v, each as 64 token rows of up to
+  // 128 channels, MN-major SWIZZLE_128B (64-channel blocks 8 KB apart)
+  static constexpr uint32_t A23 = B1_lo + 64 * K * 2;
+  static constexpr uint32_t A3_off = 2 * 64 * 128;
+  static constexpr uint32_t A23_slot = 2 * A3_off;
   static constexpr uint32_t B2 = A23 + 2 * A23_slot;    // 2 slots x 64 x 64 bf16
   static constexpr uint32_t B2_slot = 64 * 64 * 2;
   // per epilogue pair: M (fp32 64 x kAkkLd: Akk^T in the strict upper triangle,
@@ -71,9 +76,9 @@ struct IntraLayout {
   static constexpr uint32_t sInv_M = 64 * kAkkLd * 4;
   static constexpr uint32_t sInv_pair = sInv_M + 4 * kXdBlk * 4;
   static constexpr uint32_t sPart = sInv + 2 * sInv_pair;    // 2 x 4 x K floats
-  static constexpr uint32_t sBeta = sPart + 2 * 4 * K * 4;  // 2 x 64 floats: beta of the item's rows
+  static constexpr uint32_t sBeta = sPart + 2 * 4 * K * 4;  // per epilogue pair, 64 floats: beta of the item's rows
   static constexpr uint32_t bars = sBeta + 2 * 64 * 4;
-  static constexpr int kBars = 14;
+  static constexpr int kBars = 16;
   static constexpr uint32_t tmem_slot = bars + kBars * 8;
   static constexpr uint32_t abort_slot = tmem_slot + 4;
   static constexpr uint32_t total = abort_slot + 4;
@@ -91,6 +96,7 @@ enum {
   kD1Empty = 8,    // [2] epi -> MMA1: D1 read                           (128 arrivals)
   kD2Full = 10,    // [2] MMA2 -> epi: W^T/U^T ready                     (commit)
   kD2Empty = 12,   // [2] epi -> MMA2: W^T/U^T read                      (128 arrivals)
+  kVFull = 14,     // [2] TMA -> MMA2: v of the item in the A3 tile      (1 arrival + bytes)
 };
 
 // 2^x by the MUFU ex2 instruction; e^x is taken as 2^(x log2 e).
@@ -100,12 +106,14 @@ __device__ __forceinline__ float exp2f_fast(float x) {
   return y;
 }
 
-// x = hi + lo with hi = bf16(x) and lo = bf16(x - hi), on a channel pair.
-__device__ __forceinline__ void split_store2(uint8_t* hi_tile, uint8_t* lo_tile, uint32_t off, f2 x) {
+// x = hi + lo with hi = bf16(x) and lo = bf16(x - hi), on a channel pair;
+// returns the hi pair.
+__device__ __forceinline__ uint32_t split_store2(uint8_t* hi_tile, uint8_t* lo_tile, uint32_t off, f2 x) {
   const uint32_t h = f2_to_bf16x2(x);
   const f2 lo = f2_sub(x, f2_from_bf16x2(h));
   *reinterpret_cast<uint32_t*>(hi_tile + off) = h;
   *reinterpret_cast<uint32_t*>(lo_tile + off) = f2_to_bf16x2(lo);
+  return h;
 }
 
 __device__ __forceinline__ uint4 pack8(const float* f) {
@@ -163,6 +171,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
       mbar_init(&bar[kD1Empty + s], 128);
       mbar_init(&bar[kD2Full + s], 1);
       mbar_init(&bar[kD2Empty + s], 128);
+      mbar_init(&bar[kVFull + s], 1);
     }
     fence_mbar_init();
   }
@@ -182,14 +191,14 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
     const int c0 = 2 * p;
     const bool kact = c0 < K, vact = c0 < V;
     float* sPart = reinterpret_cast<float*>(sm + Lay::sPart);
-    // Byte offset of this thread's channel pair in row r of a K-major
-    // SWIZZLE_128B tile: the atom, row, 16-byte chunk and in-chunk fields
+    // Byte offset of this thread's channel pair in row r of a SWIZZLE_128B
+    // tile of 128-byte rows: the atom, row, 16-byte chunk and in-chunk fields
     // occupy disjoint bits, so the chunk's XOR with (r % 8) is one XOR with a
     // per-row constant, applied to the row's base offset.
     const uint32_t cbits = ((uint32_t(c0 & 63) >> 3) << 4) | (uint32_t(c0 & 7) << 1);
     const uint32_t rows0 = uint32_t(kRowsPerThread * quarter) * 128u;
     const uint32_t xA = uint32_t(c0 >> 6) * 128u * 128u + rows0 + cbits;  // A1, row 16*quarter
-    const uint32_t xB = uint32_t(c0 >> 6) * 64u * 128u + rows0 + cbits;   // B1, row 16*quarter
+    const uint32_t xB = uint32_t(c0 >> 6) * 64u * 128u + rows0 + cbits;   // B1, A2 and A3, row 16*quarter
     int j = 0;
     // Chunk lookups (dependent loads of the chunk table in varlen mode) run two
     // items ahead, so that neither this item's loads nor the next item's L2
@@ -207,73 +216,54 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
       const int gc = cur.y;
       const int hq = hv / grp;
       const int L = ci.L, t0 = ci.t0;
+      const int s = j & 1;
       const ChunkInfo nnci = lookup(nnx);
       if (lane == 0 && warp >= 4 && nci.valid) {
         // L2 prefetch of the next item's chunk of q, k, v and g: one TMA
         // prefetch per tensor (a box of 64 token rows of one head), issued by
-        // lane 0 of warps 4-7 (not the warps that load beta)
+        // lane 0 of warps 4-7
         const int nhv = nxt.x;
         const CUtensorMap* m = warp == 4 ? &maps.q : warp == 5 ? &maps.k : warp == 6 ? &maps.v : &maps.g;
         tma_prefetch_l2_3d(m, 0, warp < 6 ? nhv / grp : nhv, nci.t0);
       }
       // ---- loads (all in flight together)
       float2 g2[kRowsPerThread];
-      uint32_t q2[kRowsPerThread], k2[kRowsPerThread], v2[kRowsPerThread];
+      uint32_t q2[kRowsPerThread], k2[kRowsPerThread];
 #pragma unroll
       for (int rr = 0; rr < kRowsPerThread; ++rr) {
         const int i = kRowsPerThread * quarter + rr;
         g2[rr] = make_float2(0.f, 0.f);
-        q2[rr] = k2[rr] = v2[rr] = 0u;
-        if (i < L) {
+        q2[rr] = k2[rr] = 0u;
+        if (i < L && kact) {
           const size_t tq = size_t(t0 + i) * P.Hq + hq, tv = size_t(t0 + i) * P.Hv + hv;
-          if (kact) {
-            g2[rr] = __ldg(reinterpret_cast<const float2*>(gp + tv * K + c0));
-            q2[rr] = __ldg(reinterpret_cast<const uint32_t*>(reinterpret_cast<const __nv_bfloat16*>(qp) + tq * K + c0));
-            k2[rr] = __ldg(reinterpret_cast<const uint32_t*>(reinterpret_cast<const __nv_bfloat16*>(kp) + tq * K + c0));
-          }
-          if (vact)
-            v2[rr] = __ldg(reinterpret_cast<const uint32_t*>(reinterpret_cast<const __nv_bfloat16*>(vp) + tv * V + c0));
+          g2[rr] = __ldg(reinterpret_cast<const float2*>(gp + tv * K + c0));
+          q2[rr] = __ldg(reinterpret_cast<const uint32_t*>(reinterpret_cast<const __nv_bfloat16*>(qp) + tq * K + c0));
+          k2[rr] = __ldg(reinterpret_cast<const uint32_t*>(reinterpret_cast<const __nv_bfloat16*>(kp) + tq * K + c0));
         }
       }
-      // ---- beta of the item's rows, loaded once by 64 threads with the rows
-      // above, as fp32 into shared memory (read by every channel pair after the
-      // barrier below; two buffers, because the next item's loads may start
-      // before slower threads finish this one)
-      float* bt = reinterpret_cast<float*>(sm + Lay::sBeta) + (j & 1) * 64 + kRowsPerThread * quarter;
-      const float bval = (tid < 64 && tid < L) ? load_beta(beta, P.beta_fp32, size_t(t0 + tid) * P.Hv + hv) : 0.f;
       // ---- cumsum offsets across row quarters
-      float* part = sPart + (j & 1) * 4 * K;
+      float* part = sPart + s * 4 * K;
       if (kact) {
-        float2 s = make_float2(0.f, 0.f);
+        float2 sum = make_float2(0.f, 0.f);
 #pragma unroll
         for (int rr = 0; rr < kRowsPerThread; ++rr) {
-          s.x += g2[rr].x;
-          s.y += g2[rr].y;
+          sum.x += g2[rr].x;
+          sum.y += g2[rr].y;
         }
-        *reinterpret_cast<float2*>(part + quarter * K + c0) = s;
+        *reinterpret_cast<float2*>(part + quarter * K + c0) = sum;
       }
-      if (tid < 64) bt[tid - kRowsPerThread * quarter] = bval;
       named_bar_sync(1, kPrepThreads);
-      float btv[kRowsPerThread];  // beta of this thread's rows
-#pragma unroll
-      for (int q = 0; q < kRowsPerThread / 4; ++q) {
-        const float4 b4 = reinterpret_cast<const float4*>(bt)[q];
-        btv[4 * q] = b4.x;
-        btv[4 * q + 1] = b4.y;
-        btv[4 * q + 2] = b4.z;
-        btv[4 * q + 3] = b4.w;
-      }
       float2 G = make_float2(0.f, 0.f), glast = make_float2(0.f, 0.f);
       if (kact) {
 #pragma unroll
         for (int qq = 0; qq < 4; ++qq) {
-          const float2 s = *reinterpret_cast<const float2*>(part + qq * K + c0);
+          const float2 ps = *reinterpret_cast<const float2*>(part + qq * K + c0);
           if (qq < quarter) {
-            G.x += s.x;
-            G.y += s.y;
+            G.x += ps.x;
+            G.y += ps.y;
           }
-          glast.x += s.x;
-          glast.y += s.y;
+          glast.x += ps.x;
+          glast.y += ps.y;
         }
       }
       // The decay factors e^{G_r - G_i} are formed as products of q e^{G} and
@@ -284,15 +274,13 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
       const float2 gam = make_float2(__expf(glast.x), __expf(glast.y));
       const size_t head_row = size_t(gc) * P.Hv + hv;
       if (kact && quarter == 0 && out.gamma) *reinterpret_cast<float2*>(out.gamma + head_row * K + c0) = gam;
-      // ---- wait for the operand tiles to be free
+      // ---- wait for MMA1 of the previous item to release A1/B1
       if (j >= 1) wait_bar(&bar[kA1Empty], par(j - 1), abort_flag, P.status);
-      if (j >= 2) wait_bar(&bar[kA23Empty + (j & 1)], par((j >> 1) - 1), abort_flag, P.status);
-      uint8_t* A2 = sm + Lay::A23 + (j & 1) * Lay::A23_slot;
-      uint8_t* A3 = A2 + 128 * 64 * 2;
       // rows of Qg and Kg in A1: the D1 rows of Kg (Akk) land in the TMEM lanes
       // of the epilogue pair that inverts this item
-      const int qrow = 64 * (j & 1), krow = 64 - qrow;
-      // ---- gated operands
+      const int qrow = 64 * s, krow = 64 - qrow;
+      // ---- gated operands of MMA1 (and the bf16 Kg rows kept for the A2 tile)
+      uint32_t kgh[kRowsPerThread];
       if (kact) {
         f2 G2 = f2_make(G.x, G.y);
         const f2 gam2 = f2_make(gam.x, gam.y);
@@ -309,7 +297,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         const size_t qs_stride = size_t(P.Hv) * K;
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
-          float a2[2][8], kl[2][8];
+          float kl[2][8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const int rr = 8 * half + e;
@@ -326,13 +314,9 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
             const f2 Kd = f2_mul(k, eN);
             const uint32_t swr = uint32_t(rr & 7) << 4, rowr = uint32_t(rr) * 128u;
             split_store2(A1h, A1l, (xq ^ swr) + rowr, Qg);
-            split_store2(A1h, A1l, (xk ^ swr) + rowr, Kg);
+            kgh[rr] = split_store2(A1h, A1l, (xk ^ swr) + rowr, Kg);
             split_store2(B1h, B1l, (xB ^ swr) + rowr, Kd);
-            const float2 kgv = f2_split(Kg);
-            const float2 a2v = make_float2(btv[rr] * kgv.x, btv[rr] * kgv.y);
             const float2 klv = f2_split(f2_mul(Kd, gam2));
-            a2[0][e] = a2v.x;
-            a2[1][e] = a2v.y;
             kl[0][e] = klv.x;
             kl[1][e] = klv.y;
             if (i < L) {
@@ -342,35 +326,46 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
               if (out.G) *reinterpret_cast<float2*>(out.G + tok * K + c0) = f2_split(G2);
             }
           }
-          const int col = kRowsPerThread * quarter + 8 * half;
+          if (out.KlT) {
+            const int col = kRowsPerThread * quarter + 8 * half;
 #pragma unroll
-          for (int ch = 0; ch < 2; ++ch) {
-            *reinterpret_cast<uint4*>(A2 + sw128_offset(c0 + ch, col, 128)) = pack8(a2[ch]);
-            if (out.KlT)
+            for (int ch = 0; ch < 2; ++ch)
               *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(out.KlT) + (head_row * K + c0 + ch) * 64 +
                                         col) = pack8(kl[ch]);
           }
         }
       }
-      if (vact) {
+      fence_proxy_async_smem();
+      mbar_arrive(&bar[kOpndFull]);
+      // ---- A2/A3 slot s: free once MMA2 of item j - 2 has read it.  v comes
+      // by TMA (MN-major, SWIZZLE_128B); the prep writes the Kg rows.
+      if (j >= 2) wait_bar(&bar[kA23Empty + s], par((j >> 1) - 1), abort_flag, P.status);
+      uint8_t* A2 = sm + Lay::A23 + s * Lay::A23_slot;
+      uint8_t* A3 = A2 + Lay::A3_off;
+      if (warp == 6 && lane == 0) {
+        mbar_arrive_expect_tx(&bar[kVFull + s], uint32_t(V) * 64u * 2u);
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          float a3[2][8];
+        for (int a = 0; a < V / 64; ++a) tma_load_3d(A3 + a * 64 * 128, &maps.v_sw, a * 64, hv, t0, &bar[kVFull + s]);
+      }
+      if (kact) {
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int rr = 8 * half + e;
-            const float2 v = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v2[rr]));
-            a3[0][e] = btv[rr] * v.x;
-            a3[1][e] = btv[rr] * v.y;
-          }
-          const int col = kRowsPerThread * quarter + 8 * half;
-          *reinterpret_cast<uint4*>(A3 + sw128_offset(c0, col, 128)) = pack8(a3[0]);
-          *reinterpret_cast<uint4*>(A3 + sw128_offset(c0 + 1, col, 128)) = pack8(a3[1]);
+        for (int rr = 0; rr < kRowsPerThread; ++rr)
+          *reinterpret_cast<uint32_t*>(A2 + (xB ^ (uint32_t(rr & 7) << 4)) + uint32_t(rr) * 128u) = kgh[rr];
+      }
+      if (L < kChunk) {
+        // tail item: rows L..63 of the v box hold tokens of the next chunk or
+        // sequence; clear them once the copy has landed, so that U depends on
+        // this chunk's tokens alone (their W/U weights are exact zeros)
+        if (vact && kRowsPerThread * quarter + kRowsPerThread > L) {
+          wait_bar(&bar[kVFull + s], par(j >> 1), abort_flag, P.status);
+#pragma unroll
+          for (int rr = 0; rr < kRowsPerThread; ++rr)
+            if (kRowsPerThread * quarter + rr >= L)
+              *reinterpret_cast<uint32_t*>(A3 + (xB ^ (uint32_t(rr & 7) << 4)) + uint32_t(rr) * 128u) = 0u;
         }
       }
       fence_proxy_async_smem();
-      mbar_arrive(&bar[kOpndFull]);
-      mbar_arrive(&bar[kA23Full + (j & 1)]);
+      mbar_arrive(&bar[kA23Full + s]);
       ci = nci;
       nci = nnci;
       cur = nxt;
@@ -393,6 +388,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
     const bool leader = (warp & 1) == 0 && lane == 0;
     float* M = reinterpret_cast<float*>(sm + Lay::sInv + pair * Lay::sInv_pair);
     float* Xd = M + 64 * kAkkLd;
+    float* sB = reinterpret_cast<float*>(sm + Lay::sBeta) + pair * 64;  // beta of the item's rows
     constexpr uint32_t id = idesc_bf16_f32(128, 64);
     // MMA1(jj), issued by the leader of the pair that inverts item jj, once
     // every prep thread has written the item's A1/B1 tiles: D1 = [Qg; Kg] Kd^T
@@ -417,17 +413,24 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
       umma_commit(&bar[kD1Full + (jj & 1)]);
       umma_commit(&bar[kA1Empty]);
     };
-    // MMA2(jj): W^T = A2 B2^T, U^T = A3 B2^T (leader of the inverting pair)
+    // MMA2(jj): W^T = Kg^T B2^T, U^T = v^T B2^T with B2 = Akk_inv diag(beta)
+    // (leader of the inverting pair).  Kg and v are MN-major tiles of 64 token
+    // rows (the K dimension here), 64-channel blocks 8 KB apart; a K step of
+    // 16 tokens advances A by 2048 B and B2 (K-major) by 32 B.
     auto mma2 = [&](int jj) {
       const int s = jj & 1;
       wait_bar(&bar[kA23Full + s], par(jj >> 1), abort_flag, P.status);
+      wait_bar(&bar[kVFull + s], par(jj >> 1), abort_flag, P.status);
       if (jj >= 2) wait_bar(&bar[kD2Empty + s], par((jj >> 1) - 1), abort_flag, P.status);
       tc_fence_after();
-      const uint64_t a2 = sdesc_kmajor_sw128(smem_u32(sm + Lay::A23 + s * Lay::A23_slot));
+      constexpr uint32_t idmn = idesc_bf16_f32(128, 64) | kIdescAMajorMN;
+      const uint32_t a2s = smem_u32(sm + Lay::A23 + s * Lay::A23_slot);
+      const uint64_t a2 = sdesc_mnmajor_sw128(a2s, 64 * 128);
+      const uint64_t a3 = sdesc_mnmajor_sw128(a2s + Lay::A3_off, 64 * 128);
       const uint64_t b2 = sdesc_kmajor_sw128(smem_u32(sm + Lay::B2 + s * Lay::B2_slot));
       const uint32_t dW = tmem + 128 + 128 * s;
-      umma_atom4(dW, a2, b2, id, 0);
-      umma_atom4(dW + 64, a2 + (128 * 64 * 2) / 16, b2, id, 0);
+      umma_k4(dW, a2, b2, idmn, 0, 2048 / 16, 2);
+      umma_k4(dW + 64, a3, b2, idmn, 0, 2048 / 16, 2);
       umma_commit(&bar[kD2Full + s]);
       umma_commit(&bar[kA23Empty + s]);
     };
@@ -513,6 +516,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
 #pragma unroll
         for (int c = 0; c < 64; ++c)
           if (c < r) M[c * kAkkLd + r] = br * __uint_as_float(c < 32 ? xa[c] : xb[c - 32]);
+        sB[r] = br;
         named_bar_sync(pair_bar, 64);
         // X = (I + Akk)^{-1} by 16 x 16 blocks.  Diagonal blocks: forward
         // substitution in registers, thread = (block d, column c), into Xd.
@@ -607,7 +611,11 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
             u = *reinterpret_cast<const float4*>(src);
             w = *reinterpret_cast<const float4*>(src + 4);
           }
-          const float f[8] = {u.x, u.y, u.z, u.w, w.x, w.y, w.z, w.w};
+          // B2 = Akk_inv diag(beta): column c scaled by beta of row c
+          const float4 b0 = *reinterpret_cast<const float4*>(sB + c8);
+          const float4 b1 = *reinterpret_cast<const float4*>(sB + c8 + 4);
+          const float f[8] = {u.x * b0.x, u.y * b0.y, u.z * b0.z, u.w * b0.w,
+                              w.x * b1.x, w.y * b1.y, w.z * b1.z, w.w * b1.w};
           *reinterpret_cast<uint4*>(B2 + sw128_offset(r, c8, 64)) = pack8(f);
           if (inv_row) {
             *reinterpret_cast<float4*>(inv_row + c8) = u;

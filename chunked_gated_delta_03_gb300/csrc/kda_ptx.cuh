@@ -174,6 +174,42 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
   return d;
 }
 
+// Shared-memory matrix descriptor for an MN-major operand in the 128-byte
+// swizzle layout (what TMA writes for a SWIZZLE_128B box of 64 bf16 along M
+// or N): each 128-B row holds 64 consecutive M (or N) elements of one K
+// index, 8-row groups (8 consecutive K indices) are 1024 B apart (SBO), and
+// the next 64 elements along M (or N) start `lbo` bytes further on (LBO).  A
+// K step of 16 advances the start address by two row groups (2048 B).
+__device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t saddr, uint32_t lbo) {
+  uint64_t d = 0;
+  d |= uint64_t((saddr & 0x3FFFFu) >> 4);
+  d |= uint64_t((lbo & 0x3FFFFu) >> 4) << 16;  // LBO: next 64 elements along M / N
+  d |= uint64_t(1024 >> 4) << 32;               // SBO: next 8 K indices
+  d |= uint64_t(1) << 46;
+  d |= uint64_t(2) << 61;
+  return d;
+}
+
+// Instruction descriptor bit that marks the A operand as MN-major.
+constexpr uint32_t kIdescAMajorMN = 1u << 15;
+
+// Four MMAs of K = 16 with per-step descriptor increments (16-byte units):
+// 2 for a K-major SW128 operand, 128 for an MN-major one.  Only the first MMA
+// takes the caller's accumulate flag.
+__device__ __forceinline__ void umma_k4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                        uint32_t accumulate, uint32_t a_step, uint32_t b_step) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 q, %11, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %6, %3, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %8, %3, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %9, %10, %3, q;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "l"(a_desc + a_step), "l"(b_desc + b_step),
+      "l"(a_desc + 2 * a_step), "l"(b_desc + 2 * b_step), "l"(a_desc + 3 * a_step), "l"(b_desc + 3 * b_step),
+      "r"(1u)
+      : "memory");
+}
+
 // Byte offset of element (row, col) inside a K-major SWIZZLE_128B bf16 tile of
 // `rows` rows: 64-column atoms stacked along K, each rows x 128 B, with the
 // 16-byte chunk index XOR-ed by (row % 8).  Matches what TMA writes for a

@@ -68,7 +68,7 @@ def algorithmic_bytes(w, N):
     inputs = BT * (2 * Hq * K * 2 + Hv * V * 2 + Hv * K * 4 + Hv * bsz)
     h0 = N * Hv * K * V * 4 if w["initial_state"] is not None else 0
     exports = BT * Hv * (64 * 4 * 2 + K * 2 + V * 2) if w["intermediates"] else 0
-    state_ops = BT * Hv * (K * 2 + 64 * 2) + nc * Hv * K * (64 * 2 + 4)     # Qs, Aqk_b, Kl^T, gamma
+    state_ops = BT * Hv * (K * 2 + 64 * 2 + K * 2) + nc * Hv * K * 4     # Qs, Aqk_b, Kl, gamma
     wu_internal = 0 if w["intermediates"] else BT * Hv * (K * 2 + V * 2)
     outputs = BT * Hv * V * 2 + N * Hv * K * V * 4
     intra = inputs + exports + wu_internal + state_ops

@@ -59,7 +59,7 @@ bool map_rows64(CUtensorMap* m, const void* base, long long rows, int box_rows) 
 }
 
 struct Layout {
-  size_t status = 0, nc = 4, idx = 0, off = 0, order = 0, Qs = 0, Aqk_b = 0, KlT = 0, gamma = 0, W = 0, U = 0, total = 0;
+  size_t status = 0, nc = 4, idx = 0, off = 0, order = 0, Qs = 0, Aqk_b = 0, Kl = 0, gamma = 0, W = 0, U = 0, total = 0;
 };
 
 struct Shape {
@@ -114,7 +114,7 @@ Layout make_layout(const Shape& s, const KdaArgs* a, bool full) {
     if (s.varlen) L.order = take(size_t(s.N > 0 ? s.N : 1) * 4);
     L.Qs = take(size_t(s.BT) * s.Hv * s.K * 2);
     L.Aqk_b = take(size_t(s.BT) * s.Hv * 64 * 2);
-    L.KlT = take(size_t(s.nc_max) * s.Hv * s.K * 64 * 2);
+    L.Kl = take(size_t(s.BT) * s.Hv * s.K * 2);
     L.gamma = take(size_t(s.nc_max) * s.Hv * s.K * 4);
     if (!a->W) L.W = take(size_t(s.BT) * s.Hv * s.K * 2);
     if (!a->U) L.U = take(size_t(s.BT) * s.Hv * s.V * 2);
@@ -251,7 +251,7 @@ extern "C" int kda_chunk_fwd(const KdaArgs* a, void* workspace, size_t ws_bytes,
   out.G = a->G;
   out.Qs = ws + L.Qs;
   out.Aqk_b = ws + L.Aqk_b;
-  out.KlT = ws + L.KlT;
+  out.Kl = ws + L.Kl;
   out.gamma = reinterpret_cast<float*>(ws + L.gamma);
   rc = run_intra(s, a, P, out, st);
   if (rc) return rc;
@@ -264,7 +264,7 @@ extern "C" int kda_chunk_fwd(const KdaArgs* a, void* workspace, size_t ws_bytes,
       !map_tokens(&m.Qs, out.Qs, bf, 2, s.K, s.Hv, s.BT, 64, sw) ||
       !map_tokens(&m.Aqk_b, out.Aqk_b, bf, 2, 64, s.Hv, s.BT, 64, sw) ||
       !map_tokens(&m.U, out.U, bf, 2, s.V, s.Hv, s.BT, s.V, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-      !map_rows64(&m.KlT, out.KlT, (long long)s.nc_max * s.Hv * s.K, s.K))
+      !map_tokens(&m.Kl, out.Kl, bf, 2, s.K, s.Hv, s.BT, 64, sw))
     return KDA_ERR_LAUNCH;
   if (launch_state(P, m, out.gamma, a->initial_state, a->o, a->final_state, st) != cudaSuccess)
     return KDA_ERR_LAUNCH;

@@ -98,7 +98,7 @@ struct IntraOut {
   // state-pass operands (null in the standalone intra primitive)
   void* Qs;         // bf16 [BT, Hv, K]: scale * q * e^G
   void* Aqk_b;      // bf16 [BT, Hv, 64]: Aqk rounded for the output MMA
-  void* KlT;        // bf16 [nc_max, Hv, K, 64]: (k * e^{G_last - G})^T per chunk
+  void* Kl;         // bf16 [BT, Hv, K]: k * e^{G_last - G}, G_last of the token's chunk
   float* gamma;     // fp32 [nc_max, Hv, K]: e^{G_last}
 };
 
@@ -116,7 +116,7 @@ struct IntraMaps {
 };
 
 struct StateMaps {
-  CUtensorMap W, Qs, Aqk_b, U, KlT;
+  CUtensorMap W, Qs, Aqk_b, U, Kl;
 };
 
 cudaError_t launch_chunk_index(const int32_t* cu, int N, int T, int chunk, int32_t* idx, int32_t* off,

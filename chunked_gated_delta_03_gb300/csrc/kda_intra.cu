@@ -15,7 +15,7 @@
 //        Qg = q*e^G, Kg = k*e^G, Kd = k*e^{-G}, split into bf16 hi + lo and
 //        written into K-major SWIZZLE_128B tiles A1 = [Qg; Kg] (128 x K, the
 //        Kg rows first for odd items), B1 = Kd (64 x K); the state-pass
-//        operands Qs, Kl^T, gamma (and G) straight to global memory.  Then,
+//        operands Qs, Kl, gamma (and G) straight to global memory.  Then,
 //        once MMA2 of item j-2 has freed slot j%2, the bf16 Kg rows go into
 //        its A2 tile and one thread starts the TMA copy of the item's v chunk
 //        into its A3 tile (both token rows, MN-major for MMA2); a tail item
@@ -294,10 +294,12 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         __nv_bfloat16* qs_row = out.Qs ? reinterpret_cast<__nv_bfloat16*>(out.Qs) +
                                              (size_t(t0 + kRowsPerThread * quarter) * P.Hv + hv) * K + c0
                                        : nullptr;
+        __nv_bfloat16* kl_row = out.Kl ? reinterpret_cast<__nv_bfloat16*>(out.Kl) +
+                                             (size_t(t0 + kRowsPerThread * quarter) * P.Hv + hv) * K + c0
+                                       : nullptr;
         const size_t qs_stride = size_t(P.Hv) * K;
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
-          float kl[2][8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const int rr = 8 * half + e;
@@ -316,22 +318,14 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
             split_store2(A1h, A1l, (xq ^ swr) + rowr, Qg);
             kgh[rr] = split_store2(A1h, A1l, (xk ^ swr) + rowr, Kg);
             split_store2(B1h, B1l, (xB ^ swr) + rowr, Kd);
-            const float2 klv = f2_split(f2_mul(Kd, gam2));
-            kl[0][e] = klv.x;
-            kl[1][e] = klv.y;
             if (i < L) {
               const size_t tok = size_t(t0 + i) * P.Hv + hv;
               if (qs_row)
                 *reinterpret_cast<uint32_t*>(qs_row + size_t(rr) * qs_stride) = f2_to_bf16x2(f2_mul(Qg, scale2));
+              if (kl_row)
+                *reinterpret_cast<uint32_t*>(kl_row + size_t(rr) * qs_stride) = f2_to_bf16x2(f2_mul(Kd, gam2));
               if (out.G) *reinterpret_cast<float2*>(out.G + tok * K + c0) = f2_split(G2);
             }
-          }
-          if (out.KlT) {
-            const int col = kRowsPerThread * quarter + 8 * half;
-#pragma unroll
-            for (int ch = 0; ch < 2; ++ch)
-              *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(out.KlT) + (head_row * K + c0 + ch) * 64 +
-                                        col) = pack8(kl[ch]);
           }
         }
       }
@@ -480,34 +474,57 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
       tc_fence_after();
       const uint32_t d1 = tmem + 64 * s;
       if (!inverts) {
-        // Aqk row r
-        const size_t tok = size_t(t0 + r) * P.Hv + hv;
+        // Aqk row r (scale, causal mask) staged in the pair's M tile, which is
+        // free between the pair's inverses (the barrier below waits for the
+        // last reads of its previous Akk_inv export), then written out by
+        // whole rows: a warp stores full 128-byte lines instead of a 16-byte
+        // piece of 32 different rows per instruction.
+        uint32_t xa[32], xb[32];
+        tmem_ld_x32(tmem_addr(d1, 32 * q4, 0), xa);
+        tmem_ld_x32(tmem_addr(d1, 32 * q4, 32), xb);
+        tc_fence_before();
+        mbar_arrive(&bar[kD1Empty + s]);
+        named_bar_sync(pair_bar, 64);
+        float* mrow = M + r * kAkkLd;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t x[32];
-          tmem_ld_x32(tmem_addr(d1, 32 * q4, 32 * h), x);
-          if (r < L) {
-            float a[32];
+        for (int c = 0; c < 64; c += 4) {
+          float a[4];
 #pragma unroll
-            for (int c = 0; c < 32; ++c) a[c] = (32 * h + c <= r) ? P.scale * __uint_as_float(x[c]) : 0.f;
-            if (out.Aqk) {
-              float4* dst = reinterpret_cast<float4*>(out.Aqk + tok * 64 + 32 * h);
-#pragma unroll
-              for (int c = 0; c < 8; ++c) dst[c] = make_float4(a[4 * c], a[4 * c + 1], a[4 * c + 2], a[4 * c + 3]);
-            }
-            if (out.Aqk_b) {
-              uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(out.Aqk_b) + tok * 64 + 32 * h);
-#pragma unroll
-              for (int c = 0; c < 4; ++c) dst[c] = pack8(a + 8 * c);
+          for (int e = 0; e < 4; ++e)
+            a[e] = (c + e <= r) ? P.scale * __uint_as_float(c + e < 32 ? xa[c + e] : xb[c + e - 32]) : 0.f;
+          *reinterpret_cast<float4*>(mrow + c) = make_float4(a[0], a[1], a[2], a[3]);
+        }
+        named_bar_sync(pair_bar, 64);
+        if (out.Aqk) {
+          // 16 passes of 4 rows x 16 column quads
+#pragma unroll 4
+          for (int it = 0; it < 16; ++it) {
+            const int row = 4 * it + (r >> 4), c4 = 4 * (r & 15);
+            if (row < L)
+              *reinterpret_cast<float4*>(out.Aqk + (size_t(t0 + row) * P.Hv + hv) * 64 + c4) =
+                  *reinterpret_cast<const float4*>(M + row * kAkkLd + c4);
+          }
+        }
+        if (out.Aqk_b) {
+          // 8 passes of 8 rows x 8 column octets, rounded to bf16
+#pragma unroll 4
+          for (int it = 0; it < 8; ++it) {
+            const int row = 8 * it + (r >> 3), c8 = 8 * (r & 7);
+            if (row < L) {
+              const float4 u = *reinterpret_cast<const float4*>(M + row * kAkkLd + c8);
+              const float4 w = *reinterpret_cast<const float4*>(M + row * kAkkLd + c8 + 4);
+              const float f[8] = {u.x, u.y, u.z, u.w, w.x, w.y, w.z, w.w};
+              *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(out.Aqk_b) +
+                                        (size_t(t0 + row) * P.Hv + hv) * 64 + c8) = pack8(f);
             }
           }
         }
-        tc_fence_before();
-        mbar_arrive(&bar[kD1Empty + s]);
+        named_bar_sync(pair_bar, 64);
       } else {
         // Akk row r, beta-scaled and strictly masked, into the strict upper
         // triangle of M as Akk^T (M[c][r] = Akk[r][c], c < r).  The pair's
-        // previous inverse ended with a barrier after its last read of M.
+        // previous use of M (the Aqk rows it staged for the item before)
+        // ended with a barrier after its last read.
         uint32_t xa[32], xb[32];
         tmem_ld_x32(tmem_addr(d1, 32 * q4, 0), xa);
         tmem_ld_x32(tmem_addr(d1, 32 * q4, 32), xb);
@@ -601,7 +618,6 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         const int d = r >> 4;
         const float* xoff = M + r * kAkkLd;
         const float* xdia = Xd + d * kXdBlk + (r & 15) * kXdLd - 16 * d;
-        float* inv_row = (out.Akk_inv && r < L) ? out.Akk_inv + (size_t(t0 + r) * P.Hv + hv) * 64 : nullptr;
 #pragma unroll
         for (int c8 = 0; c8 < 64; c8 += 8) {
           const int blk = c8 >> 4;
@@ -617,15 +633,26 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
           const float f[8] = {u.x * b0.x, u.y * b0.y, u.z * b0.z, u.w * b0.w,
                               w.x * b1.x, w.y * b1.y, w.z * b1.z, w.w * b1.w};
           *reinterpret_cast<uint4*>(B2 + sw128_offset(r, c8, 64)) = pack8(f);
-          if (inv_row) {
-            *reinterpret_cast<float4*>(inv_row + c8) = u;
-            *reinterpret_cast<float4*>(inv_row + c8 + 4) = w;
-          }
         }
         fence_proxy_async_smem();
         named_bar_sync(pair_bar, 64);
         if (leader) mma2(j);
         __syncwarp();
+        if (out.Akk_inv) {
+          // fp32 export by whole rows (16 passes of 4 rows x 16 column quads):
+          // blocks left of the diagonal from M, the diagonal block from Xd,
+          // zeros after it
+#pragma unroll 4
+          for (int it = 0; it < 16; ++it) {
+            const int row = 4 * it + (r >> 4), c4 = 4 * (r & 15);
+            const int dr = row >> 4, blk = c4 >> 4;
+            float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (blk < dr) x = *reinterpret_cast<const float4*>(M + row * kAkkLd + c4);
+            else if (blk == dr)
+              x = *reinterpret_cast<const float4*>(Xd + dr * kXdBlk + (row & 15) * kXdLd + (c4 & 15));
+            if (row < L) *reinterpret_cast<float4*>(out.Akk_inv + (size_t(t0 + row) * P.Hv + hv) * 64 + c4) = x;
+          }
+        }
       }
       if (j >= 1) store_wu(j - 1, prev_t0, prev_L, prev_hv);
       prev_t0 = t0;

@@ -190,8 +190,9 @@ __device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t saddr, uint32_t
   return d;
 }
 
-// Instruction descriptor bit that marks the A operand as MN-major.
+// Instruction descriptor bits that mark the A / B operand as MN-major.
 constexpr uint32_t kIdescAMajorMN = 1u << 15;
+constexpr uint32_t kIdescBMajorMN = 1u << 16;
 
 // Four MMAs of K = 16 with per-step descriptor increments (16-byte units):
 // 2 for a K-major SW128 operand, 128 for an MN-major one.  Only the first MMA

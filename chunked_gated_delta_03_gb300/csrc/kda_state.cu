@@ -7,7 +7,7 @@
 // channel v, one TMEM lane per v) and all operands are K-major SWIZZLE_128B:
 //   P^T  = S^T W^T                  (M=128 v, N=64,  K=K)   TMEM cols 128b ..      (2 buffers)
 //   O^T  = S^T Qs^T                 (M=128 v, N=64,  K=K)   TMEM cols 128b+64 ..
-//   H^T  = Delta^T Kl               (M=128 v, N=K,   K=64)  TMEM cols 256 ..
+//   H^T  = Delta^T Kl               (M=128 v, N=K,   K=64)  TMEM cols 256 ..  (Kl MN-major)
 //   O^T += Delta^T Aqk^T            (M=128 v, N=64,  K=64)  TMEM cols 128b+64 ..
 // issued in that order, so that P and H, which gate the chunk chain, land first.
 // with Delta = U - W S (rows past the chunk's L valid rows forced to 0),
@@ -41,7 +41,7 @@ struct StateLayout {
   // (columns 64a..64a+63) holds the 64 W rows then the 64 Qs rows.
   static constexpr uint32_t WQ = 0;                       // 128 x K, K-major SW128
   static constexpr uint32_t Aqk = WQ + 128 * K * 2;       // 64 x 64
-  static constexpr uint32_t Kl = Aqk + 64 * 64 * 2;       // K x 64 (Kl^T rows = k)
+  static constexpr uint32_t Kl = Aqk + 64 * 64 * 2;       // 64 token rows x K, 64-channel blocks 8 KB apart
   static constexpr uint32_t stageA_bytes = ((Kl + K * 64 * 2) + 1023) / 1024 * 1024;
   // ring B stage
   static constexpr uint32_t U = 0;                        // 64 x V, plain row-major
@@ -159,7 +159,8 @@ __global__ void __launch_bounds__(kStateThreads, 1)
           tma_prefetch_l2_3d(&maps.Qs, a * 64, hv, t0);
         }
         tma_prefetch_l2_3d(&maps.Aqk_b, 0, hv, t0);
-        tma_prefetch_l2_2d(&maps.KlT, 0, (gc * P.Hv + hv) * K);
+#pragma unroll
+        for (int a = 0; a < K / 64; ++a) tma_prefetch_l2_3d(&maps.Kl, a * 64, hv, t0);
         tma_prefetch_l2_3d(&maps.U, 0, hv, t0);
         bulk_prefetch_l2(gamma + (size_t(gc) * P.Hv + hv) * K, K * 4);
       };
@@ -182,7 +183,8 @@ __global__ void __launch_bounds__(kStateThreads, 1)
           tma_load_3d(st + Lay::WQ + a * 128 * 128 + 64 * 128, &maps.Qs, a * 64, hv, t0, &fullA[sa]);
         }
         tma_load_3d(st + Lay::Aqk, &maps.Aqk_b, 0, hv, t0, &fullA[sa]);
-        tma_load_2d(st + Lay::Kl, &maps.KlT, 0, (gc * P.Hv + hv) * K, &fullA[sa]);
+#pragma unroll
+        for (int a = 0; a < K / 64; ++a) tma_load_3d(st + Lay::Kl + a * 64 * 128, &maps.Kl, a * 64, hv, t0, &fullA[sa]);
         if (c >= kStagesB) wait_bar(&emptyB[sb], (c / kStagesB - 1) & 1, abort_flag, P.status);
         uint8_t* sbp = sm + Lay::ringB + sb * Lay::stageB_bytes;
         mbar_arrive_expect_tx(&fullB[sb], Lay::txB_bytes);
@@ -210,8 +212,10 @@ __global__ void __launch_bounds__(kStateThreads, 1)
         umma_kloop(tmem + ocol, sS, 128, st + Lay::WQ + 64 * 128, 128, K / 16, id64, 0);
         wait_bar(dready, c & 1, abort_flag, P.status);
         tc_fence_after();
-        // H^T = Delta^T Kl first (it gates the next chunk), then O^T += Delta^T Aqk^T
-        umma_kloop(tmem + 256, sD, 128, st + Lay::Kl, K, 4, idK, 0);
+        // H^T = Delta^T Kl first (it gates the next chunk), then O^T += Delta^T Aqk^T.
+        // Kl is MN-major (token rows): a K step of 16 tokens is 2048 B.
+        umma_k4(tmem + 256, sdesc_kmajor_sw128(sD), sdesc_mnmajor_sw128(st + Lay::Kl, 64 * 128),
+                idK | kIdescBMajorMN, 0, 2, 2048 / 16);
         umma_commit(bar_H);
         umma_kloop(tmem + ocol, sD, 128, st + Lay::Aqk, 64, 4, id64, 1);
         umma_commit(bar_O);
@@ -268,6 +272,19 @@ __global__ void __launch_bounds__(kStateThreads, 1)
           const uint4 pk = make_uint4(pack_bf16x2(d[0], d[1]), pack_bf16x2(d[2], d[3]),
                                       pack_bf16x2(d[4], d[5]), pack_bf16x2(d[6], d[7]));
           *reinterpret_cast<uint4*>(sD + sw128_offset(v, r0 + j, 128)) = pk;
+        }
+      }
+      if (L < kChunk) {
+        // tail chunk: the Kl box's rows L..63 hold tokens of the next chunk or
+        // sequence; clear them before the state MMA, so that the state depends
+        // on this chunk's tokens alone (their Delta rows are exact zeros)
+        const int sa = c % kStagesA;
+        wait_bar(&fullA[sa], (c / kStagesA) & 1, abort_flag, P.status);
+        uint8_t* kl = sm + sa * Lay::stageA_bytes + Lay::Kl;
+        const int tail = kChunk - L, pieces = tail * (K / 64) * 8;  // 16-byte pieces
+        for (int idx = tid - 64; idx < pieces; idx += kEpiThreads) {
+          const int row = idx >> 3, blk = row / tail, rw = L + row % tail;
+          *reinterpret_cast<uint4*>(kl + blk * 64 * 128 + rw * 128 + (idx & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
         }
       }
       fence_proxy_async_smem();

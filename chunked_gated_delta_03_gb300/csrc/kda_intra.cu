@@ -20,6 +20,8 @@
 //        its A2 tile and one thread starts the TMA copy of the item's v chunk
 //        into its A3 tile (both token rows, MN-major for MMA2); a tail item
 //        clears the v rows past its last token once the copy has landed.
+//        Last, the prep warps store W/U of item j-2 from TMEM to global
+//        memory (thread = channel of its warp's TMEM lane quadrant).
 //  epi   (warps 8-11, two pairs: warps 8, 9 read TMEM lanes 0-63, warps 10,
 //        11 lanes 64-127).  Item j is inverted by the pair whose lanes hold
 //        its Kg rows of D1 (pair 1 for even j, pair 0 for odd j): its leader
@@ -33,9 +35,8 @@
 //        Akk_inv export and B2 = Akk_inv diag(beta) as the bf16 tile of slot
 //        j%2, and its leader issues MMA2(j): W^T = Kg^T B2^T, U^T = v^T B2^T
 //        (M=128, N=64, K=64, A MN-major).  The other pair exports the Aqk rows
-//        (fp32, and the bf16 copy for the state pass).  Then both pairs store
-//        their channels of W/U of item j-1 from TMEM to global memory.  The
-//        inverses of consecutive items thus run on the two pairs at once.
+//        (fp32, and the bf16 copy for the state pass).  The inverses of
+//        consecutive items thus run on the two pairs at once.
 //
 // TMEM: D1 double-buffered at columns 0 / 64; W^T, U^T double-buffered at
 // 128 / 256 (W) and +64 (U).  Shared memory: A1/B1 (single), A2/A3 and B2
@@ -95,7 +96,7 @@ enum {
   kD1Full = 6,     // [2] MMA1 -> epi: D1 ready                          (commit)
   kD1Empty = 8,    // [2] epi -> MMA1: D1 read                           (128 arrivals)
   kD2Full = 10,    // [2] MMA2 -> epi: W^T/U^T ready                     (commit)
-  kD2Empty = 12,   // [2] epi -> MMA2: W^T/U^T read                      (128 arrivals)
+  kD2Empty = 12,   // [2] prep -> MMA2: W^T/U^T read                     (256 arrivals)
   kVFull = 14,     // [2] TMA -> MMA2: v of the item in the A3 tile      (1 arrival + bytes)
 };
 
@@ -170,7 +171,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
       mbar_init(&bar[kD1Full + s], 1);
       mbar_init(&bar[kD1Empty + s], 128);
       mbar_init(&bar[kD2Full + s], 1);
-      mbar_init(&bar[kD2Empty + s], 128);
+      mbar_init(&bar[kD2Empty + s], kPrepThreads);
       mbar_init(&bar[kVFull + s], 1);
     }
     fence_mbar_init();
@@ -208,6 +209,37 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
     auto lookup = [&](int2 c) {
       return c.y < P.nc_max ? chunk_info(P, c.y) : ChunkInfo{0, 0, 0, 0, false};
     };
+    // W/U of item jj from TMEM straight to global memory: thread = channel
+    // 32*(warp%4) + lane (the warp's TMEM lane quadrant), warps 0-3 taking
+    // tokens 0-31 and warps 4-7 tokens 32-63 (a warp writes 64 contiguous
+    // bytes per token).  Run two items late, when MMA2 of the item is done.
+    auto store_wu = [&](int jj, int3 u) {
+      const int sb = jj & 1;
+      wait_bar(&bar[kD2Full + sb], par(jj >> 1), abort_flag, P.status);
+      tc_fence_after();
+      const uint32_t dW = tmem + 128 + 128 * sb;
+      const int q4 = warp & 3, th = warp >> 2;
+      const int ch = 32 * q4 + lane;
+#pragma unroll 1
+      for (int part = 0; part < 2; ++part) {
+        const int D = part == 0 ? K : V;
+        uint32_t x[32];
+        tmem_ld_x32(tmem_addr(dW + 64 * part + 32 * th, 32 * q4, 0), x);
+        if (32 * q4 < D) {
+          __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(part == 0 ? out.W : out.U) +
+                               (size_t(u.x + 32 * th) * P.Hv + u.z) * D + ch;
+          const size_t stride = size_t(P.Hv) * D;
+#pragma unroll
+          for (int t = 0; t < 32; ++t) {
+            if (32 * th + t < u.y) *dst = __float2bfloat16_rn(__uint_as_float(x[t]));
+            dst += stride;
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&bar[kD2Empty + sb]);
+    };
+    int3 hist[2] = {make_int3(0, 0, 0), make_int3(0, 0, 0)};  // (t0, L, hv) of items j-2, j-1
     int2 cur = first, nxt = advance(first), nnx = advance(nxt);
     ChunkInfo ci = lookup(cur);
     ChunkInfo nci = lookup(nxt);
@@ -360,6 +392,9 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
       }
       fence_proxy_async_smem();
       mbar_arrive(&bar[kA23Full + s]);
+      if (j >= 2) store_wu(j - 2, hist[0]);
+      hist[0] = hist[1];
+      hist[1] = make_int3(t0, L, hv);
       ci = nci;
       nci = nnci;
       cur = nxt;
@@ -367,6 +402,8 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
       nnx = advance(nnx);
       ++j;
     }
+    if (j >= 2) store_wu(j - 2, hist[0]);
+    if (j >= 1) store_wu(j - 1, hist[1]);
 
   } else {
     // ================================================================ epi
@@ -428,35 +465,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
       umma_commit(&bar[kD2Full + s]);
       umma_commit(&bar[kA23Empty + s]);
     };
-    // W/U of item jj from TMEM straight to global memory: thread = channel
-    // 32*q4 + lane, one bf16 per token (a warp writes 64 contiguous bytes).
-    auto store_wu = [&](int jj, int t0, int L, int hv) {
-      const int s = jj & 1;
-      wait_bar(&bar[kD2Full + s], par(jj >> 1), abort_flag, P.status);
-      tc_fence_after();
-      const uint32_t dW = tmem + 128 + 128 * s;
-      const int ch = 32 * q4 + lane;
-#pragma unroll 1
-      for (int part = 0; part < 2; ++part) {
-        const int D = part == 0 ? K : V;
-        uint32_t x[64];
-        tmem_ld_x64(tmem_addr(dW + 64 * part, 32 * q4, 0), x);
-        if (32 * q4 < D) {
-          __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(part == 0 ? out.W : out.U) +
-                               (size_t(t0) * P.Hv + hv) * D + ch;
-          const size_t stride = size_t(P.Hv) * D;
-#pragma unroll
-          for (int t = 0; t < 64; ++t) {
-            if (t < L) *dst = __float2bfloat16_rn(__uint_as_float(x[t]));
-            dst += stride;
-          }
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(&bar[kD2Empty + s]);
-    };
     int j = 0;
-    int prev_t0 = 0, prev_L = 0, prev_hv = 0;
     for (int2 cur = first; cur.y < P.nc_max; cur = advance(cur)) {
       const int hv = cur.x;
       const ChunkInfo ci = chunk_info(P, cur.y);
@@ -614,7 +623,9 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         }
         // row r of X: bf16 B2 operand row and the fp32 export row (blocks left
         // of the diagonal from M, the diagonal block from Xd, zeros after it)
+        // (once MMA2 of the pair's previous item has finished reading the slot)
         uint8_t* B2 = sm + Lay::B2 + s * Lay::B2_slot;
+        if (j >= 2) wait_bar(&bar[kD2Full + s], par((j >> 1) - 1), abort_flag, P.status);
         const int d = r >> 4;
         const float* xoff = M + r * kAkkLd;
         const float* xdia = Xd + d * kXdBlk + (r & 15) * kXdLd - 16 * d;
@@ -654,13 +665,8 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
           }
         }
       }
-      if (j >= 1) store_wu(j - 1, prev_t0, prev_L, prev_hv);
-      prev_t0 = t0;
-      prev_L = L;
-      prev_hv = hv;
       ++j;
     }
-    if (j >= 1) store_wu(j - 1, prev_t0, prev_L, prev_hv);
   }
   tc_fence_before();
   __syncthreads();

@@ -59,6 +59,7 @@ class KdaArgs(ctypes.Structure):
         ("U", ctypes.c_void_p),
         ("G", ctypes.c_void_p),
         ("profile_events", ctypes.c_void_p),
+        ("QG", ctypes.c_void_p),
     ]
 
 

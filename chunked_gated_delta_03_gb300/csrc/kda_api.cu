@@ -135,7 +135,7 @@ int check_arch() {
 int check_inputs(const KdaArgs* a, const void* ws, long long BT) {
   if (BT > 0 && (!a->q || !a->k || !a->v || !a->g || !a->beta)) return KDA_ERR_INVALID;
   const void* ptrs[] = {a->q, a->k, a->v, a->g, a->beta, a->cu_seqlens, a->initial_state, a->o,
-                        a->final_state, a->Aqk, a->Akk_inv, a->W, a->U, a->G};
+                        a->final_state, a->Aqk, a->Akk_inv, a->W, a->U, a->G, a->QG};
   for (const void* p : ptrs)
     if (p && !aligned16(p)) return KDA_ERR_MISALIGNED;
   if (ws && (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1))) return KDA_ERR_MISALIGNED;
@@ -249,6 +249,7 @@ extern "C" int kda_chunk_fwd(const KdaArgs* a, void* workspace, size_t ws_bytes,
   out.W = a->W ? a->W : ws + L.W;
   out.U = a->U ? a->U : ws + L.U;
   out.G = a->G;
+  out.QG = a->QG;
   out.Qs = ws + L.Qs;
   out.Aqk_b = ws + L.Aqk_b;
   out.Kl = ws + L.Kl;
@@ -287,6 +288,7 @@ extern "C" int kda_fwd_intra(const KdaArgs* a, void* workspace, size_t ws_bytes,
   out.W = a->W;
   out.U = a->U;
   out.G = a->G;
+  out.QG = a->QG;
   return run_intra(s, a, P, out, st);
 }
 

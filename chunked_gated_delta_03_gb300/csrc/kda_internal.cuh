@@ -95,6 +95,7 @@ struct IntraOut {
   void* W;          // bf16 [BT, Hv, K]  (required)
   void* U;          // bf16 [BT, Hv, V]  (required)
   float* G;         // fp32 [BT, Hv, K]  (may be null)
+  void* QG;         // bf16 [BT, Hv, K]: q * e^G (may be null)
   // state-pass operands (null in the standalone intra primitive)
   void* Qs;         // bf16 [BT, Hv, K]: scale * q * e^G
   void* Aqk_b;      // bf16 [BT, Hv, 64]: Aqk rounded for the output MMA

@@ -15,7 +15,7 @@
 //        Qg = q*e^G, Kg = k*e^G, Kd = k*e^{-G}, split into bf16 hi + lo and
 //        written into K-major SWIZZLE_128B tiles A1 = [Qg; Kg] (128 x K, the
 //        Kg rows first for odd items), B1 = Kd (64 x K); the state-pass
-//        operands Qs, Kl, gamma (and G) straight to global memory.  Then,
+//        operands Qs, Kl, gamma (and G, QG) straight to global memory.  Then,
 //        once MMA2 of item j-2 has freed slot j%2, the bf16 Kg rows go into
 //        its A2 tile and one thread starts the TMA copy of the item's v chunk
 //        into its A3 tile (both token rows, MN-major for MMA2); a tail item
@@ -132,7 +132,7 @@ __device__ __forceinline__ float load_beta(const void* beta, int fp32, size_t i)
 // Parity of the wait for the n-th completion (n >= 0) of a barrier.
 __device__ __forceinline__ uint32_t par(int n) { return uint32_t(n) & 1u; }
 
-template <int K, int V>
+template <int K, int V, bool kQG>
 __global__ void __launch_bounds__(kIntraThreads, 1)
     intra_kernel(const Problem P, const void* __restrict__ qp, const void* __restrict__ kp,
                  const void* __restrict__ vp, const float* __restrict__ gp, const void* __restrict__ beta,
@@ -357,6 +357,9 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
               if (kl_row)
                 *reinterpret_cast<uint32_t*>(kl_row + size_t(rr) * qs_stride) = f2_to_bf16x2(f2_mul(Kd, gam2));
               if (out.G) *reinterpret_cast<float2*>(out.G + tok * K + c0) = f2_split(G2);
+              if constexpr (kQG)
+                *reinterpret_cast<uint32_t*>(reinterpret_cast<__nv_bfloat16*>(out.QG) + tok * K + c0) =
+                    f2_to_bf16x2(Qg);
             }
           }
         }
@@ -676,11 +679,11 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
   }
 }
 
-template <int K, int V>
+template <int K, int V, bool kQG>
 cudaError_t launch_intra_t(const Problem& P, const IntraInputs& in, const IntraOut& out, const IntraMaps& maps,
                            cudaStream_t s) {
   constexpr uint32_t smem = IntraLayout<K, V>::bytes;
-  cudaError_t e = cudaFuncSetAttribute(intra_kernel<K, V>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = cudaFuncSetAttribute(intra_kernel<K, V, kQG>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const long long items = (long long)P.nc_max * P.Hv;
   if (items <= 0) return cudaSuccess;
@@ -688,7 +691,7 @@ cudaError_t launch_intra_t(const Problem& P, const IntraInputs& in, const IntraO
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   const unsigned grid = unsigned(items < sms ? items : sms);
-  intra_kernel<K, V><<<grid, kIntraThreads, smem, s>>>(P, in.q, in.k, in.v, in.g, in.beta, out, maps);
+  intra_kernel<K, V, kQG><<<grid, kIntraThreads, smem, s>>>(P, in.q, in.k, in.v, in.g, in.beta, out, maps);
   return cudaGetLastError();
 }
 
@@ -696,10 +699,18 @@ cudaError_t launch_intra_t(const Problem& P, const IntraInputs& in, const IntraO
 
 cudaError_t launch_intra(const Problem& P, const IntraInputs& in, const IntraOut& out, const IntraMaps& maps,
                          cudaStream_t s) {
-  if (P.K == 128 && P.V == 128) return launch_intra_t<128, 128>(P, in, out, maps, s);
-  if (P.K == 128 && P.V == 64) return launch_intra_t<128, 64>(P, in, out, maps, s);
-  if (P.K == 64 && P.V == 128) return launch_intra_t<64, 128>(P, in, out, maps, s);
-  if (P.K == 64 && P.V == 64) return launch_intra_t<64, 64>(P, in, out, maps, s);
+  // The optional QG export has its own instantiations: any code added to the
+  // prep's row loop changes its register allocation, so the usual path
+  // carries none of it.
+  const bool qg = out.QG != nullptr;
+  if (P.K == 128 && P.V == 128)
+    return qg ? launch_intra_t<128, 128, true>(P, in, out, maps, s) : launch_intra_t<128, 128, false>(P, in, out, maps, s);
+  if (P.K == 128 && P.V == 64)
+    return qg ? launch_intra_t<128, 64, true>(P, in, out, maps, s) : launch_intra_t<128, 64, false>(P, in, out, maps, s);
+  if (P.K == 64 && P.V == 128)
+    return qg ? launch_intra_t<64, 128, true>(P, in, out, maps, s) : launch_intra_t<64, 128, false>(P, in, out, maps, s);
+  if (P.K == 64 && P.V == 64)
+    return qg ? launch_intra_t<64, 64, true>(P, in, out, maps, s) : launch_intra_t<64, 64, false>(P, in, out, maps, s);
   return cudaErrorInvalidValue;
 }
 

@@ -71,12 +71,13 @@ def _contig(*ts):
 
 
 def chunk_kda_fwd(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=None,
-                  output_final_state=True, return_intermediates=False, return_G=False):
+                  output_final_state=True, return_intermediates=False, return_G=False, return_QG=False):
     """Chunked KDA forward.  Returns (o, final_state, intermediates).
 
     ``intermediates`` is None unless ``return_intermediates`` (then a dict with
     Aqk, Akk_inv [B,T,Hv,64] fp32 and W [B,T,Hv,K], U [B,T,Hv,V] bf16) or
-    ``return_G`` (adds G [B,T,Hv,K] fp32).  ``final_state`` is None unless
+    ``return_G`` (adds G [B,T,Hv,K] fp32) or ``return_QG`` (adds the gated
+    query QG = q * e^G [B,T,Hv,K] bf16).  ``final_state`` is None unless
     ``output_final_state``.
     """
     q, k, v, g, beta, cu_seqlens, initial_state = _contig(q, k, v, g, beta, cu_seqlens, initial_state)
@@ -84,7 +85,7 @@ def chunk_kda_fwd(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=N
     dev = q.device
     o = torch.empty(B, T, Hv, V, dtype=torch.bfloat16, device=dev)
     final = torch.empty(N, Hv, K, V, dtype=torch.float32, device=dev) if output_final_state else None
-    inter = {} if (return_intermediates or return_G) else None
+    inter = {} if (return_intermediates or return_G or return_QG) else None
     if return_intermediates:
         inter["Aqk"] = torch.empty(B, T, Hv, _CHUNK, dtype=torch.float32, device=dev)
         inter["Akk_inv"] = torch.empty(B, T, Hv, _CHUNK, dtype=torch.float32, device=dev)
@@ -92,10 +93,13 @@ def chunk_kda_fwd(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=N
         inter["U"] = torch.empty(B, T, Hv, V, dtype=torch.bfloat16, device=dev)
     if return_G:
         inter["G"] = torch.empty(B, T, Hv, K, dtype=torch.float32, device=dev)
+    if return_QG:
+        inter["QG"] = torch.empty(B, T, Hv, K, dtype=torch.bfloat16, device=dev)
     a.o, a.final_state = _ptr(o), _ptr(final)
     if inter:
         a.Aqk, a.Akk_inv = _ptr(inter.get("Aqk")), _ptr(inter.get("Akk_inv"))
         a.W, a.U, a.G = _ptr(inter.get("W")), _ptr(inter.get("U")), _ptr(inter.get("G"))
+        a.QG = _ptr(inter.get("QG"))
     ws_bytes = _lib.kda_workspace_size(a)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     rc = _lib.kda_chunk_fwd(a, ws.data_ptr(), ws_bytes, torch.cuda.current_stream(dev).cuda_stream)
@@ -104,8 +108,8 @@ def chunk_kda_fwd(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=N
     return o, final, inter
 
 
-def chunk_kda_fwd_intra(q, k, v, g, beta, scale=None, cu_seqlens=None, return_G=False):
-    """The standalone intra-chunk primitive: dict with Aqk, Akk_inv, W, U (and G)."""
+def chunk_kda_fwd_intra(q, k, v, g, beta, scale=None, cu_seqlens=None, return_G=False, return_QG=False):
+    """The standalone intra-chunk primitive: dict with Aqk, Akk_inv, W, U (and G, QG)."""
     q, k, v, g, beta, cu_seqlens = _contig(q, k, v, g, beta, cu_seqlens)
     a, (B, T, Hq, Hv, K, V, N) = make_args(q, k, v, g, beta, scale, None, cu_seqlens)
     dev = q.device
@@ -117,8 +121,11 @@ def chunk_kda_fwd_intra(q, k, v, g, beta, scale=None, cu_seqlens=None, return_G=
     }
     if return_G:
         out["G"] = torch.empty(B, T, Hv, K, dtype=torch.float32, device=dev)
+    if return_QG:
+        out["QG"] = torch.empty(B, T, Hv, K, dtype=torch.bfloat16, device=dev)
     a.Aqk, a.Akk_inv, a.W, a.U = (_ptr(out[n]) for n in ("Aqk", "Akk_inv", "W", "U"))
     a.G = _ptr(out.get("G"))
+    a.QG = _ptr(out.get("QG"))
     ws_bytes = _lib.kda_workspace_size(a)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     rc = _lib.kda_fwd_intra(a, ws.data_ptr(), ws_bytes, torch.cuda.current_stream(dev).cuda_stream)

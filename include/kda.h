@@ -112,6 +112,11 @@ typedef struct KdaArgs {
    * `stream` before the first kernel, after the intra-chunk kernel and after
    * the state/output kernel (kda_chunk_fwd); NULL = no events. */
   void* const* profile_events;
+  /* optional output (both entry points; NULL = not written): the gated query
+   * QG = q * e^G, bf16 [B, T, Hv, K], row t of value head hv from q of its
+   * q/k head and the in-chunk cumsum G of the value head's gates (the
+   * "optional QG" of cuLA PR #131, Summary).  Rounded from the FP32 product. */
+  void* QG;
 } KdaArgs;
 
 typedef KdaArgs KdaFwdArgs;

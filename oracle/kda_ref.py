@@ -227,8 +227,10 @@ def kda_chunked(q, k, v, g, beta, scale, initial_state=None, cu_seqlens=None,
 
     Returns a dict with o [B,T,Hv,V], final_state [N,Hv,K,V], and the
     token-major intermediates Aqk, Akk, Akk_inv [B,T,Hv,C], W [B,T,Hv,K],
-    U [B,T,Hv,V], G [B,T,Hv,K].  ``heads`` restricts the work to a subset of
-    value heads (the other heads stay zero).
+    U [B,T,Hv,V], G [B,T,Hv,K] and the gated query QG = q * e^G [B,T,Hv,K]
+    (the optional QG output of cuLA PR #131, Summary; per value head, from the
+    q/k head it reads).  ``heads`` restricts the work to a subset of value
+    heads (the other heads stay zero).
     """
     q, k, v, g, beta = map(_f64, (q, k, v, g, beta))
     S_init = _f64(initial_state)
@@ -247,6 +249,7 @@ def kda_chunked(q, k, v, g, beta, scale, initial_state=None, cu_seqlens=None,
         "W": np.zeros((B, T, Hv, K)),
         "U": np.zeros((B, T, Hv, V)),
         "G": np.zeros((B, T, Hv, K)),
+        "QG": np.zeros((B, T, Hv, K)),
     }
     for n, (b, bos, eos) in enumerate(seqs):
         for hv in hv_list:
@@ -269,6 +272,7 @@ def kda_chunked(q, k, v, g, beta, scale, initial_state=None, cu_seqlens=None,
                 out["W"][b, t0:t1, hv] = W
                 out["U"][b, t0:t1, hv] = U
                 out["G"][b, t0:t1, hv] = G_c
+                out["QG"][b, t0:t1, hv] = q_c * np.exp(G_c)
             out["final_state"][n, hv] = S
     return out
 

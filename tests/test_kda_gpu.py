@@ -24,6 +24,9 @@ TOL_STATE = dict(max_abs=2e-2, rel=5e-3)
 TOL_WU = dict(atol=2e-2, rtol=1e-2, rel=5e-3)
 TOL_FP32 = dict(rel=1e-4)
 TOL_G = dict(rel=1e-5)
+# QG = q e^G is rounded once from an FP32 product to bf16 (8 significant
+# bits): |err| <= 2^-8 |ref| plus the FP32 exp error
+TOL_QG = dict(atol=1e-6, rtol=2.0 ** -8 + 1e-5, rel=3e-3)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -64,10 +67,10 @@ def _cuda(inp):
     return {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
 
 
-def _ours(inp, inter=True, G=False):
+def _ours(inp, inter=True, G=False, QG=False):
     return ops.chunk_kda_fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["scale"],
                              inp["initial_state"], inp["cu_seqlens"], output_final_state=True,
-                             return_intermediates=inter, return_G=G)
+                             return_intermediates=inter, return_G=G, return_QG=QG)
 
 
 def _check(name, got, want, max_abs=None, rel=None, atol=None, rtol=None):
@@ -101,6 +104,8 @@ def _compare(inp, out, want, heads=None, inter=True):
         _check("U", _np(im["U"][:, :, sel]), want["U"], **TOL_WU)
         if "G" in im:
             _check("G", _np(im["G"][:, :, sel]), want["G"], **TOL_G)
+        if "QG" in im:
+            _check("QG", _np(im["QG"][:, :, sel]), want["QG"], **TOL_QG)
 
 
 SMALL_CASES = {
@@ -118,7 +123,7 @@ SMALL_CASES = {
 def test_small_cases_match_oracle(case):
     inp = make_inputs(WORKLOADS["tiny"], seed=100 + len(case), **SMALL_CASES[case])
     want = _oracle(inp)
-    out = _ours(_cuda(inp), inter=True, G=True)
+    out = _ours(_cuda(inp), inter=True, G=True, QG=True)
     _compare(inp, out, want, inter=True)
 
 
@@ -140,9 +145,9 @@ def test_outputs_without_intermediates(case):
 def test_intra_primitive_matches_oracle_and_full_path():
     inp = _cuda(make_inputs(WORKLOADS["tiny"], seed=7, **SMALL_CASES["varlen"]))
     intra = ops.chunk_kda_fwd_intra(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["scale"],
-                                    inp["cu_seqlens"], return_G=True)
-    _, _, im = _ours(inp, inter=True, G=True)
-    for key in ("Aqk", "Akk_inv", "W", "U", "G"):
+                                    inp["cu_seqlens"], return_G=True, return_QG=True)
+    _, _, im = _ours(inp, inter=True, G=True, QG=True)
+    for key in ("Aqk", "Akk_inv", "W", "U", "G", "QG"):
         assert torch.equal(intra[key], im[key]), key
     want = _oracle({k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()})
     _check("Akk_inv", _np(intra["Akk_inv"]), want["Akk_inv"], **TOL_FP32)

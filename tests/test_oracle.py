@@ -347,3 +347,49 @@ def test_chunk_indices_reject_unsorted():
 def test_chunk_indices_empty():
     idx, off = ref.prepare_chunk_indices(np.array([0], np.int32), 64)
     assert idx.shape == (0, 2) and off.tolist() == [0]
+
+
+# ---------------------------------------------------------------------------
+# the optional gated query QG = q * e^G (cuLA PR #131, Summary: optional QG)
+# ---------------------------------------------------------------------------
+
+def test_gated_query_closed_form_constant_gates():
+    # Gates constant in time (per value head and channel): row r of a chunk
+    # (counting from 0 at the chunk start, the count restarting at every chunk
+    # and sequence) carries q * exp((r + 1) * g).  Value head hv reads the q
+    # of q/k head hv // (Hv // Hq).  Packed varlen with ragged sequences.
+    rng = np.random.default_rng(91)
+    lens = [70, 5, 130]
+    T, Hq, Hv, K, V = sum(lens), 2, 4, 8, 4
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    q = rng.standard_normal((1, T, Hq, K))
+    k = rng.standard_normal((1, T, Hq, K)) * 0.1
+    v = rng.standard_normal((1, T, Hv, V))
+    gc = -rng.uniform(0.01, 0.2, size=(Hv, K))
+    g = np.broadcast_to(gc, (1, T, Hv, K)).copy()
+    beta = np.full((1, T, Hv), 0.5)
+    out = ref.kda_chunked(q, k, v, g, beta, 0.3, None, cu, chunk_size=64)
+    want = np.zeros((1, T, Hv, K))
+    for bos, eos in zip(cu[:-1], cu[1:]):
+        for t in range(bos, eos):
+            r = (t - bos) % 64
+            for hv in range(Hv):
+                want[0, t, hv] = q[0, t, hv // (Hv // Hq)] * np.exp((r + 1) * gc[hv])
+    assert _close(out["QG"], want)
+
+
+def test_gated_query_brute_force_products():
+    # Random gates: QG[t] = q[t] * prod_{j = chunk start .. t} exp(g_j), a
+    # running product of per-token factors (no cumsum of logs).
+    q, k, v, g, beta, _ = _rand_inputs(92, B=2, T=150, Hq=1, Hv=2, K=4, V=3, with_h0=False)
+    out = ref.kda_chunked(q, k, v, g, beta, 0.5, None, None, chunk_size=64)
+    want = np.zeros_like(out["QG"])
+    for b in range(2):
+        for hv in range(2):
+            prod = np.ones(4)
+            for t in range(150):
+                if t % 64 == 0:
+                    prod = np.ones(4)
+                prod = prod * np.exp(g[b, t, hv])
+                want[b, t, hv] = q[b, t, 0] * prod
+    assert _close(out["QG"], want)

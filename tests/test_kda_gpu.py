@@ -297,6 +297,32 @@ def test_empty_inputs():
     assert torch.equal(final, inp["initial_state"])
 
 
+def test_nonfinite_values_stay_in_their_sequence():
+    # Packed varlen: sequence 0 ends in a tail chunk (tokens 64-99, L = 36)
+    # whose 64-row TMA boxes (v in the intra kernel, Kl in the state kernel)
+    # also cover the first tokens of sequence 1.  NaN / Inf planted in v and k
+    # of those tokens must not reach sequence 0: its o and final state match
+    # the oracle run on sequence 0 alone.
+    inp = make_inputs(WORKLOADS["tiny"], seed=61, lengths=(100, 50), Hq=2, Hv=2, K=128, V=128,
+                      initial_state=True)
+    bad = {k: (v.clone() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    bad["v"][0, 110, 1, 5] = float("nan")
+    bad["v"][0, 120, 0, :] = float("inf")
+    bad["k"][0, 105, 0, 7] = float("nan")
+    bad["k"][0, 126, 1, :] = float("inf")
+    o, final, _ = _ours(_cuda(bad), inter=True)
+    seq0 = make_inputs(WORKLOADS["tiny"], seed=61, lengths=(100, 50), Hq=2, Hv=2, K=128, V=128,
+                       initial_state=True)
+    for key in ("q", "k", "v", "g", "beta"):
+        seq0[key] = seq0[key][:, :100]
+    seq0["initial_state"] = seq0["initial_state"][:1]
+    seq0["cu_seqlens"] = None
+    seq0["T"] = 100
+    want = _oracle(seq0)
+    _check("o", _np(o[:, :100]), want["o"], **TOL_STATE)
+    _check("final_state", _np(final[:1]), want["final_state"], **TOL_STATE)
+
+
 def test_replay_is_bitwise_deterministic():
     inp = _cuda(make_inputs(WORKLOADS["varlen_16k"], varlen_total=4096, Hq=8, Hv=8))
     first = _ours(inp, inter=True)

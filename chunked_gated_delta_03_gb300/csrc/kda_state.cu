@@ -20,7 +20,7 @@
 // Warp roles: warp 0 issues TMA loads (and L2 prefetches one ring depth
 // ahead, so that the stage loads hit L2), warp 1 issues the MMAs, warps 2-9
 // (256 threads, two per TMEM lane quadrant) run the epilogue.  Two rings: ring A (MMA operands [W; Qs],
-// Aqk, Kl^T; 2 stages) is released by the MMAs' own completion, so the next
+// Aqk, Kl as token rows; 2 stages) is released by the MMAs' own completion, so the next
 // loads start mid-chunk; ring B (U and gamma, read by the epilogue; 3 stages)
 // is released by the epilogue.
 #include "kda_internal.cuh"

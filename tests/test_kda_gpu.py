@@ -4,9 +4,10 @@ Tolerances (floating point): o and final_state max |err| <= 2e-2 and relative
 L2 <= 5e-3 (bf16 I/O); Akk_inv and Aqk relative L2 <= 1e-4 (FP32 outputs of an
 ~FP32-accurate hi/lo-split product and an FP32 inverse); W, U elementwise
 |err| <= 2e-2 + 1e-2 |ref| and relative L2 <= 5e-3 (bf16 outputs whose values
-reach several units: a bf16 half-ulp alone is 2^-9 |x|, and the Akk_inv and
-beta*k*e^G / beta*v operands are bf16 too); G relative L2 <= 1e-5 (FP32
-cumsum).  Chunk indices and offsets: bit-exact.
+reach several units: a bf16 half-ulp alone is 2^-9 |x|, and their MMA
+operands k*e^G, v and Akk_inv diag(beta) are bf16 too); G relative L2 <= 1e-5
+(FP32 cumsum); QG = q*e^G elementwise |err| <= 2^-8 |ref| + 1e-6 (one bf16
+rounding of an FP32 product).  Chunk indices and offsets: bit-exact.
 """
 
 import numpy as np

@@ -39,7 +39,7 @@ G_r = sum_{j<=r} g_j the inclusive in-chunk cumsum):
   Aqk[r,i] = scale sum_c q_r[c] k_i[c] e^{G_r[c]-G_i[c]} (i <= r), and the
   state after the chunk is Diag(e^{G_last}) S0 + (K*e^{G_last-G})^T Delta.
 
-Readings taken where the pages are silent (each one is listed in the design doc):
+Readings taken where the pages are silent:
   * Akk is stored positive, beta-scaled and strictly lower triangular;
     Akk_inv = (I + Akk)^{-1} includes its unit diagonal and is zero above it.
   * Aqk includes ``scale`` and its diagonal.

@@ -60,6 +60,7 @@ class KdaArgs(ctypes.Structure):
         ("G", ctypes.c_void_p),
         ("profile_events", ctypes.c_void_p),
         ("QG", ctypes.c_void_p),
+        ("intra_tf32", ctypes.c_int32),
     ]
 
 

@@ -155,6 +155,7 @@ Problem make_problem(const Shape& s, const KdaArgs* a, uint8_t* ws, const Layout
   P.nc_max = s.nc_max;
   P.varlen = s.varlen;
   P.beta_fp32 = a->beta_dtype == KDA_DTYPE_FP32;
+  P.tf32 = a->intra_tf32 != 0;
   P.scale = a->scale;
   P.cu = a->cu_seqlens;
   P.status = reinterpret_cast<int32_t*>(ws + L.status);

@@ -21,6 +21,7 @@ struct Problem {
   int nc_max;        // upper bound on the chunk count (grid size)
   int varlen;        // 1 when cu_seqlens is given
   int beta_fp32;     // 1: beta is fp32, 0: bf16
+  int tf32;          // 1: Aqk / Akk from TF32 operands in one MMA pass
   float scale;
   const int32_t* cu;         // varlen: cu_seqlens
   const int32_t* chunk_idx;  // varlen: [nc, 2] (sequence, chunk within sequence)

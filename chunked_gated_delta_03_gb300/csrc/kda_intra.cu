@@ -132,7 +132,7 @@ __device__ __forceinline__ float load_beta(const void* beta, int fp32, size_t i)
 // Parity of the wait for the n-th completion (n >= 0) of a barrier.
 __device__ __forceinline__ uint32_t par(int n) { return uint32_t(n) & 1u; }
 
-template <int K, int V, bool kQG>
+template <int K, int V, bool kQG, bool kTF32>
 __global__ void __launch_bounds__(kIntraThreads, 1)
     intra_kernel(const Problem P, const void* __restrict__ qp, const void* __restrict__ kp,
                  const void* __restrict__ vp, const float* __restrict__ gp, const void* __restrict__ beta,
@@ -198,8 +198,13 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
     // per-row constant, applied to the row's base offset.
     const uint32_t cbits = ((uint32_t(c0 & 63) >> 3) << 4) | (uint32_t(c0 & 7) << 1);
     const uint32_t rows0 = uint32_t(kRowsPerThread * quarter) * 128u;
-    const uint32_t xA = uint32_t(c0 >> 6) * 128u * 128u + rows0 + cbits;  // A1, row 16*quarter
-    const uint32_t xB = uint32_t(c0 >> 6) * 64u * 128u + rows0 + cbits;   // B1, A2 and A3, row 16*quarter
+    // (with TF32 operands A1 and B1 hold fp32 rows of 32 channels per atom)
+    const uint32_t cbits32 = ((uint32_t(c0 & 31) >> 2) << 4) | (uint32_t(c0 & 3) << 2);
+    const uint32_t xA = kTF32 ? uint32_t(c0 >> 5) * 128u * 128u + rows0 + cbits32
+                              : uint32_t(c0 >> 6) * 128u * 128u + rows0 + cbits;  // A1, row 16*quarter
+    const uint32_t xB1 = kTF32 ? uint32_t(c0 >> 5) * 64u * 128u + rows0 + cbits32
+                               : uint32_t(c0 >> 6) * 64u * 128u + rows0 + cbits;  // B1, row 16*quarter
+    const uint32_t xB = uint32_t(c0 >> 6) * 64u * 128u + rows0 + cbits;   // A2 and A3, row 16*quarter
     int j = 0;
     // Chunk lookups (dependent loads of the chunk table in varlen mode) run two
     // items ahead, so that neither this item's loads nor the next item's L2
@@ -347,9 +352,17 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
             const f2 Kg = f2_mul(k, eG);
             const f2 Kd = f2_mul(k, eN);
             const uint32_t swr = uint32_t(rr & 7) << 4, rowr = uint32_t(rr) * 128u;
-            split_store2(A1h, A1l, (xq ^ swr) + rowr, Qg);
-            kgh[rr] = split_store2(A1h, A1l, (xk ^ swr) + rowr, Kg);
-            split_store2(B1h, B1l, (xB ^ swr) + rowr, Kd);
+            if constexpr (kTF32) {
+              // fp32 tiles spanning the hi and lo areas, rounded to TF32
+              *reinterpret_cast<unsigned long long*>(A1h + (xq ^ swr) + rowr) = f2_to_tf32x2(Qg);
+              *reinterpret_cast<unsigned long long*>(A1h + (xk ^ swr) + rowr) = f2_to_tf32x2(Kg);
+              *reinterpret_cast<unsigned long long*>(B1h + (xB1 ^ swr) + rowr) = f2_to_tf32x2(Kd);
+              kgh[rr] = f2_to_bf16x2(Kg);
+            } else {
+              split_store2(A1h, A1l, (xq ^ swr) + rowr, Qg);
+              kgh[rr] = split_store2(A1h, A1l, (xk ^ swr) + rowr, Kg);
+              split_store2(B1h, B1l, (xB1 ^ swr) + rowr, Kd);
+            }
             if (i < L) {
               const size_t tok = size_t(t0 + i) * P.Hv + hv;
               if (qs_row)
@@ -438,12 +451,19 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
       const uint32_t d1 = tmem + 64 * (jj & 1);
       // atoms of 64 channels: 128 rows of A1 (1024 descriptor units apart), 64
       // rows of B1 (512 apart)
+      if constexpr (kTF32) {
+        // one pass on the fp32 tiles: atoms of 32 channels
+        constexpr uint32_t idt = idesc_tf32_f32(128, 64);
 #pragma unroll
-      for (int at = 0; at < K / 64; ++at) umma_atom4(d1, a_hi + at * 1024, b_hi + at * 512, id, at > 0);
+        for (int at = 0; at < K / 32; ++at) umma_atom4_tf32(d1, a_hi + at * 1024, b_hi + at * 512, idt, at > 0);
+      } else {
 #pragma unroll
-      for (int at = 0; at < K / 64; ++at) umma_atom4(d1, a_hi + at * 1024, b_lo + at * 512, id, 1);
+        for (int at = 0; at < K / 64; ++at) umma_atom4(d1, a_hi + at * 1024, b_hi + at * 512, id, at > 0);
 #pragma unroll
-      for (int at = 0; at < K / 64; ++at) umma_atom4(d1, a_lo + at * 1024, b_hi + at * 512, id, 1);
+        for (int at = 0; at < K / 64; ++at) umma_atom4(d1, a_hi + at * 1024, b_lo + at * 512, id, 1);
+#pragma unroll
+        for (int at = 0; at < K / 64; ++at) umma_atom4(d1, a_lo + at * 1024, b_hi + at * 512, id, 1);
+      }
       umma_commit(&bar[kD1Full + (jj & 1)]);
       umma_commit(&bar[kA1Empty]);
     };
@@ -679,11 +699,12 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
   }
 }
 
-template <int K, int V, bool kQG>
+template <int K, int V, bool kQG, bool kTF32>
 cudaError_t launch_intra_t(const Problem& P, const IntraInputs& in, const IntraOut& out, const IntraMaps& maps,
                            cudaStream_t s) {
   constexpr uint32_t smem = IntraLayout<K, V>::bytes;
-  cudaError_t e = cudaFuncSetAttribute(intra_kernel<K, V, kQG>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e =
+      cudaFuncSetAttribute(intra_kernel<K, V, kQG, kTF32>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const long long items = (long long)P.nc_max * P.Hv;
   if (items <= 0) return cudaSuccess;
@@ -691,7 +712,7 @@ cudaError_t launch_intra_t(const Problem& P, const IntraInputs& in, const IntraO
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   const unsigned grid = unsigned(items < sms ? items : sms);
-  intra_kernel<K, V, kQG><<<grid, kIntraThreads, smem, s>>>(P, in.q, in.k, in.v, in.g, in.beta, out, maps);
+  intra_kernel<K, V, kQG, kTF32><<<grid, kIntraThreads, smem, s>>>(P, in.q, in.k, in.v, in.g, in.beta, out, maps);
   return cudaGetLastError();
 }
 
@@ -702,15 +723,35 @@ cudaError_t launch_intra(const Problem& P, const IntraInputs& in, const IntraOut
   // The optional QG export has its own instantiations: any code added to the
   // prep's row loop changes its register allocation, so the usual path
   // carries none of it.
+  // The TF32 precision option likewise.
   const bool qg = out.QG != nullptr;
+  if (P.tf32) {
+    if (P.K == 128 && P.V == 128)
+      return qg ? launch_intra_t<128, 128, true, true>(P, in, out, maps, s)
+                : launch_intra_t<128, 128, false, true>(P, in, out, maps, s);
+    if (P.K == 128 && P.V == 64)
+      return qg ? launch_intra_t<128, 64, true, true>(P, in, out, maps, s)
+                : launch_intra_t<128, 64, false, true>(P, in, out, maps, s);
+    if (P.K == 64 && P.V == 128)
+      return qg ? launch_intra_t<64, 128, true, true>(P, in, out, maps, s)
+                : launch_intra_t<64, 128, false, true>(P, in, out, maps, s);
+    if (P.K == 64 && P.V == 64)
+      return qg ? launch_intra_t<64, 64, true, true>(P, in, out, maps, s)
+                : launch_intra_t<64, 64, false, true>(P, in, out, maps, s);
+    return cudaErrorInvalidValue;
+  }
   if (P.K == 128 && P.V == 128)
-    return qg ? launch_intra_t<128, 128, true>(P, in, out, maps, s) : launch_intra_t<128, 128, false>(P, in, out, maps, s);
+    return qg ? launch_intra_t<128, 128, true, false>(P, in, out, maps, s)
+              : launch_intra_t<128, 128, false, false>(P, in, out, maps, s);
   if (P.K == 128 && P.V == 64)
-    return qg ? launch_intra_t<128, 64, true>(P, in, out, maps, s) : launch_intra_t<128, 64, false>(P, in, out, maps, s);
+    return qg ? launch_intra_t<128, 64, true, false>(P, in, out, maps, s)
+              : launch_intra_t<128, 64, false, false>(P, in, out, maps, s);
   if (P.K == 64 && P.V == 128)
-    return qg ? launch_intra_t<64, 128, true>(P, in, out, maps, s) : launch_intra_t<64, 128, false>(P, in, out, maps, s);
+    return qg ? launch_intra_t<64, 128, true, false>(P, in, out, maps, s)
+              : launch_intra_t<64, 128, false, false>(P, in, out, maps, s);
   if (P.K == 64 && P.V == 64)
-    return qg ? launch_intra_t<64, 64, true>(P, in, out, maps, s) : launch_intra_t<64, 64, false>(P, in, out, maps, s);
+    return qg ? launch_intra_t<64, 64, true, false>(P, in, out, maps, s)
+              : launch_intra_t<64, 64, false, false>(P, in, out, maps, s);
   return cudaErrorInvalidValue;
 }
 

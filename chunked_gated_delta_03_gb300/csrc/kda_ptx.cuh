@@ -159,6 +159,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
 }
 
+// Instruction descriptor of tcgen05.mma kind::tf32 with TF32 A/B (fp32 data
+// in shared memory, read with a 10-bit mantissa), FP32 D and both operands
+// K-major: the A/B format fields hold TF32 (2).
+__host__ __device__ constexpr uint32_t idesc_tf32_f32(int M, int N) {
+  return (1u << 4) | (2u << 7) | (2u << 10) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
+}
+
 // Shared-memory matrix descriptor for a K-major operand in the 128-byte
 // swizzle layout: rows of 128 B (64 bf16 along K), 8-row core groups 1024 B
 // apart (SBO), version 1 at bit 46, layout type 2 (SWIZZLE_128B) at bits 61-63.
@@ -267,6 +274,23 @@ __device__ __forceinline__ void umma_atom4(uint32_t d_tmem, uint64_t a_desc, uin
       : "memory");
 }
 
+// Four TF32 MMAs of K = 8 over one 128-byte swizzle atom (32 fp32 along K),
+// issued from one asm block; a K step of 8 fp32 (32 bytes) adds 2 to the
+// descriptors' address field.  Only the first MMA takes the caller's
+// accumulate flag.
+__device__ __forceinline__ void umma_atom4_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 q, %11, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %5, %6, %3, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %7, %8, %3, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %9, %10, %3, q;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "l"(a_desc + 2), "l"(b_desc + 2), "l"(a_desc + 4),
+      "l"(b_desc + 4), "l"(a_desc + 6), "l"(b_desc + 6), "r"(1u)
+      : "memory");
+}
+
 // Warp-collective TMEM load: lane i of the warp reads TMEM lane (taddr.lane + i),
 // 16 consecutive 32-bit columns starting at taddr.col, and waits for completion
 // inside the same asm block so no use of the registers can be hoisted above it.
@@ -355,6 +379,18 @@ __device__ __forceinline__ f2 f2_mul(f2 a, f2 b) {
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
   return r;
 }
+// f32x2 rounded to the nearest TF32 values (10-bit mantissa, ties away from
+// zero), as the 64-bit pattern of the pair: a tensor core reading fp32 data
+// as TF32 drops the low mantissa bits, which would bias every product toward
+// zero.
+__device__ __forceinline__ unsigned long long f2_to_tf32x2(f2 a) {
+  const float2 x = f2_split(a);
+  uint32_t lo, hi;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(lo) : "f"(x.x));
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(hi) : "f"(x.y));
+  return (static_cast<unsigned long long>(hi) << 32) | lo;
+}
+
 // bf16x2 (low half = first element) -> f32x2
 __device__ __forceinline__ f2 f2_from_bf16x2(uint32_t u) {
   return f2_make(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));

@@ -71,13 +71,16 @@ def _contig(*ts):
 
 
 def chunk_kda_fwd(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=None,
-                  output_final_state=True, return_intermediates=False, return_G=False, return_QG=False):
+                  output_final_state=True, return_intermediates=False, return_G=False, return_QG=False,
+                  tf32=False):
     """Chunked KDA forward.  Returns (o, final_state, intermediates).
 
     ``intermediates`` is None unless ``return_intermediates`` (then a dict with
     Aqk, Akk_inv [B,T,Hv,64] fp32 and W [B,T,Hv,K], U [B,T,Hv,V] bf16) or
     ``return_G`` (adds G [B,T,Hv,K] fp32) or ``return_QG`` (adds the gated
-    query QG = q * e^G [B,T,Hv,K] bf16).  ``final_state`` is None unless
+    query QG = q * e^G [B,T,Hv,K] bf16).  ``tf32`` selects the single-pass
+    TF32 intra-chunk products (faster; Akk_inv near 5e-5 instead of 1e-6
+    relative L2).  ``final_state`` is None unless
     ``output_final_state``.
     """
     q, k, v, g, beta, cu_seqlens, initial_state = _contig(q, k, v, g, beta, cu_seqlens, initial_state)
@@ -96,6 +99,7 @@ def chunk_kda_fwd(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=N
     if return_QG:
         inter["QG"] = torch.empty(B, T, Hv, K, dtype=torch.bfloat16, device=dev)
     a.o, a.final_state = _ptr(o), _ptr(final)
+    a.intra_tf32 = 1 if tf32 else 0
     if inter:
         a.Aqk, a.Akk_inv = _ptr(inter.get("Aqk")), _ptr(inter.get("Akk_inv"))
         a.W, a.U, a.G = _ptr(inter.get("W")), _ptr(inter.get("U")), _ptr(inter.get("G"))
@@ -108,7 +112,8 @@ def chunk_kda_fwd(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=N
     return o, final, inter
 
 
-def chunk_kda_fwd_intra(q, k, v, g, beta, scale=None, cu_seqlens=None, return_G=False, return_QG=False):
+def chunk_kda_fwd_intra(q, k, v, g, beta, scale=None, cu_seqlens=None, return_G=False, return_QG=False,
+                        tf32=False):
     """The standalone intra-chunk primitive: dict with Aqk, Akk_inv, W, U (and G, QG)."""
     q, k, v, g, beta, cu_seqlens = _contig(q, k, v, g, beta, cu_seqlens)
     a, (B, T, Hq, Hv, K, V, N) = make_args(q, k, v, g, beta, scale, None, cu_seqlens)
@@ -126,6 +131,7 @@ def chunk_kda_fwd_intra(q, k, v, g, beta, scale=None, cu_seqlens=None, return_G=
     a.Aqk, a.Akk_inv, a.W, a.U = (_ptr(out[n]) for n in ("Aqk", "Akk_inv", "W", "U"))
     a.G = _ptr(out.get("G"))
     a.QG = _ptr(out.get("QG"))
+    a.intra_tf32 = 1 if tf32 else 0
     ws_bytes = _lib.kda_workspace_size(a)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     rc = _lib.kda_fwd_intra(a, ws.data_ptr(), ws_bytes, torch.cuda.current_stream(dev).cuda_stream)

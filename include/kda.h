@@ -117,6 +117,14 @@ typedef struct KdaArgs {
    * q/k head and the in-chunk cumsum G of the value head's gates (the
    * "optional QG" of cuLA PR #131, Summary).  Rounded from the FP32 product. */
   void* QG;
+  /* Precision option of the intra-chunk products (both entry points).  0:
+   * Aqk and Akk from bf16 hi/lo operand pairs in three MMA passes (relative
+   * L2 error of Akk_inv near 1e-6 against FP64).  Nonzero: one MMA pass on
+   * TF32 operands rounded to nearest, a few per cent faster, with Akk_inv
+   * near 5e-5 and Aqk near 3e-4 (the pages' SM100 path keeps TF32 conversion
+   * points, cuLA PR #131, Numerical behavior).  o, the final state, W and U
+   * stay within the same bars either way. */
+  int32_t intra_tf32;
 } KdaArgs;
 
 typedef KdaArgs KdaFwdArgs;

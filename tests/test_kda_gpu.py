@@ -25,6 +25,9 @@ TOL_STATE = dict(max_abs=2e-2, rel=5e-3)
 TOL_WU = dict(atol=2e-2, rtol=1e-2, rel=5e-3)
 TOL_FP32 = dict(rel=1e-4)
 TOL_G = dict(rel=1e-5)
+# The TF32 option rounds the gated q and k factors to TF32 (10-bit mantissa)
+# before one MMA pass: a few 1e-4 relative error in Aqk
+TOL_AQK_TF32 = dict(rel=1e-3)
 # QG = q e^G is rounded once from an FP32 product to bf16 (8 significant
 # bits): |err| <= 2^-8 |ref| plus the FP32 exp error
 TOL_QG = dict(atol=1e-6, rtol=2.0 ** -8 + 1e-5, rel=3e-3)
@@ -68,10 +71,10 @@ def _cuda(inp):
     return {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
 
 
-def _ours(inp, inter=True, G=False, QG=False):
+def _ours(inp, inter=True, G=False, QG=False, tf32=False):
     return ops.chunk_kda_fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["scale"],
                              inp["initial_state"], inp["cu_seqlens"], output_final_state=True,
-                             return_intermediates=inter, return_G=G, return_QG=QG)
+                             return_intermediates=inter, return_G=G, return_QG=QG, tf32=tf32)
 
 
 def _check(name, got, want, max_abs=None, rel=None, atol=None, rtol=None):
@@ -126,6 +129,24 @@ def test_small_cases_match_oracle(case):
     want = _oracle(inp)
     out = _ours(_cuda(inp), inter=True, G=True, QG=True)
     _compare(inp, out, want, inter=True)
+
+
+@pytest.mark.parametrize("case", ["tiny", "ragged_k64_v128", "ragged_k128_v64", "gva_init", "varlen"])
+def test_tf32_option_matches_oracle(case):
+    # The TF32 option (single-pass Aqk / Akk on TF32 operands) keeps Akk_inv
+    # within the specified 1e-4; Aqk takes the TF32 bar; everything else the
+    # default bars.
+    inp = make_inputs(WORKLOADS["tiny"], seed=300 + len(case), **SMALL_CASES[case])
+    want = _oracle(inp)
+    o, final, im = _ours(_cuda(inp), inter=True, G=True, QG=True, tf32=True)
+    _check("o", _np(o), want["o"], **TOL_STATE)
+    _check("final_state", _np(final), want["final_state"], **TOL_STATE)
+    _check("Akk_inv", _np(im["Akk_inv"]), want["Akk_inv"], **TOL_FP32)
+    _check("Aqk", _np(im["Aqk"]), want["Aqk"], **TOL_AQK_TF32)
+    _check("W", _np(im["W"]), want["W"], **TOL_WU)
+    _check("U", _np(im["U"]), want["U"], **TOL_WU)
+    _check("G", _np(im["G"]), want["G"], **TOL_G)
+    _check("QG", _np(im["QG"]), want["QG"], **TOL_QG)
 
 
 @pytest.mark.parametrize("case", ["gva_init", "varlen"])

@@ -74,6 +74,7 @@ __all__ = [
     "recompute_w_u",
     "chunk_state_output",
     "kda_chunked",
+    "gated_query",
     "prepare_lens",
     "prepare_chunk_indices",
 ]
@@ -221,6 +222,13 @@ def chunk_state_output(S0, q_c, k_c, G_c, Aqk, W, U, scale):
     return o, S1
 
 
+def gated_query(q_c, G_c):
+    """The optional QG output of cuLA PR #131 (Summary: "optional QG"): the
+    query of each row gated by its in-chunk cumulative log-gate, q * e^G.
+    The pages say no more; it is read per value head, without ``scale``."""
+    return q_c * np.exp(G_c)
+
+
 def kda_chunked(q, k, v, g, beta, scale, initial_state=None, cu_seqlens=None,
                 chunk_size=64, heads=None):
     """Chunked KDA forward in FP64 (O2), with every intermediate.
@@ -272,7 +280,7 @@ def kda_chunked(q, k, v, g, beta, scale, initial_state=None, cu_seqlens=None,
                 out["W"][b, t0:t1, hv] = W
                 out["U"][b, t0:t1, hv] = U
                 out["G"][b, t0:t1, hv] = G_c
-                out["QG"][b, t0:t1, hv] = q_c * np.exp(G_c)
+                out["QG"][b, t0:t1, hv] = gated_query(q_c, G_c)
             out["final_state"][n, hv] = S
     return out
 

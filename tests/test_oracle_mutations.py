@@ -26,6 +26,8 @@ PIN_CALLS = [
     pins.test_gva_equals_mha_with_repeated_qk,
     pins.test_continuation_across_calls,
     lambda: pins.test_chunk_indices_brute_force([1, 63, 64, 65, 0, 129, 3], 64),
+    pins.test_gated_query_closed_form_constant_gates,
+    pins.test_gated_query_brute_force_products,
 ]
 
 
@@ -41,7 +43,7 @@ def _failing_pins():
 
 _orig = {name: getattr(ref, name) for name in (
     "chunk_local_cumsum", "intra_chunk_matrices", "invert_unit_lower",
-    "recompute_w_u", "chunk_state_output", "kda_recurrent", "prepare_chunk_indices")}
+    "recompute_w_u", "chunk_state_output", "kda_recurrent", "prepare_chunk_indices", "gated_query")}
 
 
 def _exclusive_cumsum(g):
@@ -123,6 +125,18 @@ def _recurrent_decay_after_update(q, k, v, g, beta, scale, initial_state=None,
     return o, fin
 
 
+def _qg_negated_gate(q_c, G_c):
+    return q_c * np.exp(-G_c)
+
+
+def _qg_previous_row(q_c, G_c):
+    return _orig["gated_query"](q_c, _exclusive_cumsum(np.diff(G_c, axis=0, prepend=0.0)))
+
+
+def _qg_scaled(q_c, G_c):
+    return _orig["gated_query"](q_c, G_c) * q_c.shape[-1] ** -0.5
+
+
 def _indices_floor(cu, C):
     lens = ref.prepare_lens(cu)
     pairs, off = [], [0]
@@ -148,6 +162,9 @@ MUTATIONS = {
     "Aqk transposed": ("chunk_state_output", _aqk_transposed),
     "recurrence decays after the update": ("kda_recurrent", _recurrent_decay_after_update),
     "chunk count rounds down": ("prepare_chunk_indices", _indices_floor),
+    "QG with the gate negated": ("gated_query", _qg_negated_gate),
+    "QG with the previous row's cumsum": ("gated_query", _qg_previous_row),
+    "QG carrying scale": ("gated_query", _qg_scaled),
 }
 
 

@@ -28,15 +28,19 @@
 //        issues MMA1(j),
 //          D1 = A1_hi B1_hi^T + A1_hi B1_lo^T + A1_lo B1_hi^T
 //        (M=128, N=64, ~FP32-accurate; the Qg rows give Aqk/scale, the Kg
-//        rows Akk/beta); the pair copies its Akk rows, beta-scaled and
+//        rows Akk/beta; with the TF32 option the prep writes fp32 operands
+//        rounded to TF32 across the hi and lo areas instead, and MMA1 is one
+//        pass of kind::tf32 MMAs); the pair copies its Akk rows, beta-scaled and
 //        strictly masked, into shared memory as Akk^T, inverts (I + Akk) in
 //        FP32 by 16 x 16 blocks (forward substitution on the diagonal blocks,
-//        then three block diagonals of T = A X, X = -X_ii T), writes the fp32
-//        Akk_inv export and B2 = Akk_inv diag(beta) as the bf16 tile of slot
-//        j%2, and its leader issues MMA2(j): W^T = Kg^T B2^T, U^T = v^T B2^T
-//        (M=128, N=64, K=64, A MN-major).  The other pair exports the Aqk rows
-//        (fp32, and the bf16 copy for the state pass).  The inverses of
-//        consecutive items thus run on the two pairs at once.
+//        then three block diagonals of T = A X, X = -X_ii T), writes
+//        B2 = Akk_inv diag(beta) as the bf16 tile of slot j%2, its leader
+//        issues MMA2(j): W^T = Kg^T B2^T, U^T = v^T B2^T (M=128, N=64, K=64,
+//        A MN-major), and the pair writes the fp32 Akk_inv export by whole
+//        rows.  The other pair stages the Aqk rows (scale, causal mask) in its
+//        idle Akk^T tile and writes them by whole rows (fp32, and the bf16 copy
+//        for the state pass).  The inverses of consecutive items thus run on
+//        the two pairs at once.
 //
 // TMEM: D1 double-buffered at columns 0 / 64; W^T, U^T double-buffered at
 // 128 / 256 (W) and +64 (U).  Shared memory: A1/B1 (single), A2/A3 and B2
@@ -49,7 +53,7 @@ namespace kda {
 namespace {
 
 constexpr int kPrepWarps = 8;
-constexpr int kEpiWarp0 = kPrepWarps;     // warps 8..11; lane 0 of warp 8 also issues the MMAs
+constexpr int kEpiWarp0 = kPrepWarps;     // warps 8..11: two pairs, whose leaders issue the MMAs
 constexpr int kIntraThreads = (kPrepWarps + 4) * 32;
 constexpr int kPrepThreads = kPrepWarps * 32;
 constexpr int kAkkLd = 68;  // fp32 row stride of the Akk tile (conflict-free float4 rows)
@@ -95,7 +99,7 @@ enum {
   kA23Empty = 4,   // [2] MMA2 done reading the A2/A3 slot -> prep       (commit)
   kD1Full = 6,     // [2] MMA1 -> epi: D1 ready                          (commit)
   kD1Empty = 8,    // [2] epi -> MMA1: D1 read                           (128 arrivals)
-  kD2Full = 10,    // [2] MMA2 -> epi: W^T/U^T ready                     (commit)
+  kD2Full = 10,    // [2] MMA2 -> prep (W/U stores), inverting pair (B2 reuse)  (commit)
   kD2Empty = 12,   // [2] prep -> MMA2: W^T/U^T read                     (256 arrivals)
   kVFull = 14,     // [2] TMA -> MMA2: v of the item in the A3 tile      (1 arrival + bytes)
 };

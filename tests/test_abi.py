@@ -81,6 +81,7 @@ def _args(**kw):
     (dict(q=0), _lib.KDA_ERR_INVALID),
     (dict(o=0), _lib.KDA_ERR_INVALID),
     (dict(q=(1 << 20) + 8), _lib.KDA_ERR_MISALIGNED),
+    (dict(QG=(1 << 20) + 4), _lib.KDA_ERR_MISALIGNED),   # the optional gated-query output
     (dict(cu_seqlens=1 << 20, B=2, N=1), _lib.KDA_ERR_INVALID),  # varlen needs B == 1
 ])
 def test_chunk_fwd_rejects_bad_arguments(lib, kw, code):
@@ -104,6 +105,14 @@ def test_workspace_size_accounts_for_missing_w_u(lib):
     without = _args()
     # the state pass needs W and U: without caller buffers they live in the workspace
     assert _lib.kda_workspace_size(without) - _lib.kda_workspace_size(with_wu) >= 2 * 128 * 2 * 64 * 2
+
+
+def test_workspace_size_ignores_optional_exports_and_precision(lib):
+    # QG and the TF32 option change what the intra kernel writes and how it
+    # forms Aqk / Akk, not the workspace the call needs
+    base = _lib.kda_workspace_size(_args())
+    assert _lib.kda_workspace_size(_args(QG=1 << 20)) == base
+    assert _lib.kda_workspace_size(_args(intra_tf32=1)) == base
 
 
 def test_intra_requires_its_outputs(lib):

@@ -21,9 +21,13 @@ KDA_ERR_WORKSPACE = -6
 KDA_ERR_BAD_SEQLENS = -16
 KDA_ERR_TIMEOUT = -17
 KDA_ERR_GATE_RANGE = -18
+KDA_ERR_BAD_CHUNK_TABLE = -19
 KDA_MAX_CHUNK_LOG_DECAY = 60.0
 KDA_DTYPE_BF16 = 0
 KDA_DTYPE_FP32 = 1
+KDA_PATH_AUTO = 0
+KDA_PATH_FUSED = 1
+KDA_PATH_TWO_PASS = 2
 
 EXPORTS = ("kda_workspace_size", "kda_chunk_fwd", "kda_fwd_intra", "kda_prepare_chunk_indices",
            "kda_get_device_status", "kda_status_string", "kda_chunk_fwd_static_scratch", "kda_check_bounded_wait")
@@ -61,6 +65,9 @@ class KdaArgs(ctypes.Structure):
         ("profile_events", ctypes.c_void_p),
         ("QG", ctypes.c_void_p),
         ("intra_tf32", ctypes.c_int32),
+        ("path", ctypes.c_int32),
+        ("chunk_indices", ctypes.c_void_p),
+        ("chunk_offsets", ctypes.c_void_p),
     ]
 
 

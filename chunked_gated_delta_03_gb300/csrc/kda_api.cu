@@ -4,6 +4,7 @@
 // kda_get_device_status, whose job is to read the status word back.
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "kda_internal.cuh"
@@ -45,19 +46,6 @@ bool map_tokens(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int es
              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Tiled map over a [rows, 64] bf16 matrix with SWIZZLE_128B boxes of (64, box_rows).
-bool map_rows64(CUtensorMap* m, const void* base, long long rows, int box_rows) {
-  auto enc = encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {64, cuuint64_t(rows)};
-  cuuint64_t strides[1] = {128};
-  cuuint32_t box[2] = {64, cuuint32_t(box_rows)};
-  cuuint32_t es[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 struct Layout {
   size_t status = 0, nc = 4, idx = 0, off = 0, order = 0, Qs = 0, Aqk_b = 0, Kl = 0, gamma = 0, W = 0, U = 0, total = 0;
 };
@@ -67,6 +55,10 @@ struct Shape {
   long long BT;
 };
 
+// What a call runs: the intra-chunk primitive alone, the two-pass forward, or
+// the fused forward.
+enum class Mode { kIntra, kTwoPass, kFused };
+
 // Validates the sizes (not the pointers) and fills the derived counts.
 int check_shape(const KdaArgs* a, Shape* s) {
   if (!a) return KDA_ERR_INVALID;
@@ -75,6 +67,7 @@ int check_shape(const KdaArgs* a, Shape* s) {
   if (a->B < 1 || a->T < 0 || a->Hq < 1 || a->Hv < 1 || a->Hv % a->Hq != 0) return KDA_ERR_INVALID;
   if ((a->K != 64 && a->K != 128) || (a->V != 64 && a->V != 128)) return KDA_ERR_UNSUPPORTED;
   if (a->beta_dtype != KDA_DTYPE_BF16 && a->beta_dtype != KDA_DTYPE_FP32) return KDA_ERR_INVALID;
+  if ((a->chunk_indices == nullptr) != (a->chunk_offsets == nullptr)) return KDA_ERR_INVALID;
   s->B = a->B;
   s->T = a->T;
   s->Hq = a->Hq;
@@ -94,11 +87,26 @@ int check_shape(const KdaArgs* a, Shape* s) {
     s->nc_max = a->B * s->NT;
   }
   // 32-bit TMA coordinates and grid sizes
-  if (s->BT >= (1ll << 31) || (long long)s->nc_max * s->Hv * s->K >= (1ll << 31)) return KDA_ERR_UNSUPPORTED;
+  if (s->BT >= (1ll << 31) || (long long)s->nc_max * s->Hv * s->K >= (1ll << 31) ||
+      (long long)s->N * s->Hv >= (1ll << 31))
+    return KDA_ERR_UNSUPPORTED;
   return KDA_OK;
 }
 
-Layout make_layout(const Shape& s, const KdaArgs* a, bool full) {
+// The forward's kernels for these arguments (enum kda_path).
+int forward_mode(const KdaArgs* a, Mode* m) {
+  switch (a->path) {
+    case KDA_PATH_AUTO: *m = a->intra_tf32 ? Mode::kTwoPass : Mode::kFused; return KDA_OK;
+    case KDA_PATH_FUSED:
+      if (a->intra_tf32) return KDA_ERR_UNSUPPORTED;
+      *m = Mode::kFused;
+      return KDA_OK;
+    case KDA_PATH_TWO_PASS: *m = Mode::kTwoPass; return KDA_OK;
+    default: return KDA_ERR_INVALID;
+  }
+}
+
+Layout make_layout(const Shape& s, const KdaArgs* a, Mode mode) {
   Layout L;
   size_t p = kAlign;  // header: status word, chunk count
   auto take = [&p](size_t bytes) {
@@ -106,12 +114,12 @@ Layout make_layout(const Shape& s, const KdaArgs* a, bool full) {
     p = align_up(p + bytes);
     return at;
   };
-  if (s.varlen) {
+  if (s.varlen && mode != Mode::kFused && !a->chunk_indices) {
     L.idx = take(size_t(s.nc_max > 0 ? s.nc_max : 1) * 2 * 4);
     L.off = take(size_t(s.N + 1) * 4);
   }
-  if (full) {
-    if (s.varlen) L.order = take(size_t(s.N > 0 ? s.N : 1) * 4);
+  if (s.varlen && mode != Mode::kIntra) L.order = take(size_t(s.N > 0 ? s.N : 1) * 4);
+  if (mode == Mode::kTwoPass) {
     L.Qs = take(size_t(s.BT) * s.Hv * s.K * 2);
     L.Aqk_b = take(size_t(s.BT) * s.Hv * 64 * 2);
     L.Kl = take(size_t(s.BT) * s.Hv * s.K * 2);
@@ -123,12 +131,43 @@ Layout make_layout(const Shape& s, const KdaArgs* a, bool full) {
   return L;
 }
 
-int check_arch() {
-  int dev = 0, major = 0, minor = 0;
+// Device facts queried once per device: whether it is sm_103, and its SM count.
+struct DeviceInfo {
+  int dev = -1, sms = 0;
+};
+
+int device_info(DeviceInfo* out) {
+  static std::atomic<int> state[kMaxDevicesCached];  // 0 unknown, 1 sm_103, -1 other
+  static std::atomic<int> sm_count[kMaxDevicesCached];
+  int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KDA_ERR_ARCH;
-  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return KDA_ERR_ARCH;
-  if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return KDA_ERR_ARCH;
-  return (major == 10 && minor == 3) ? KDA_OK : KDA_ERR_ARCH;
+  if (dev >= 0 && dev < kMaxDevicesCached && state[dev].load(std::memory_order_acquire) != 0) {
+    if (state[dev].load(std::memory_order_relaxed) < 0) return KDA_ERR_ARCH;
+    out->dev = dev;
+    out->sms = sm_count[dev].load(std::memory_order_relaxed);
+    return KDA_OK;
+  }
+  int major = 0, minor = 0, sms = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return KDA_ERR_ARCH;
+  }
+  const bool ok = major == 10 && minor == 3;
+  if (dev >= 0 && dev < kMaxDevicesCached) {
+    sm_count[dev].store(sms, std::memory_order_relaxed);
+    state[dev].store(ok ? 1 : -1, std::memory_order_release);
+  }
+  if (!ok) return KDA_ERR_ARCH;
+  out->dev = dev;
+  out->sms = sms;
+  return KDA_OK;
+}
+
+int check_arch() {
+  DeviceInfo d;
+  return device_info(&d);
 }
 
 // Inputs may be NULL only when there are no tokens (empty tensors have no storage).
@@ -136,6 +175,9 @@ int check_inputs(const KdaArgs* a, const void* ws, long long BT) {
   if (BT > 0 && (!a->q || !a->k || !a->v || !a->g || !a->beta)) return KDA_ERR_INVALID;
   const void* ptrs[] = {a->q, a->k, a->v, a->g, a->beta, a->cu_seqlens, a->initial_state, a->o,
                         a->final_state, a->Aqk, a->Akk_inv, a->W, a->U, a->G, a->QG};
+  // the chunk table is read with 4-byte loads only
+  if ((reinterpret_cast<uintptr_t>(a->chunk_indices) | reinterpret_cast<uintptr_t>(a->chunk_offsets)) & 3u)
+    return KDA_ERR_MISALIGNED;
   for (const void* p : ptrs)
     if (p && !aligned16(p)) return KDA_ERR_MISALIGNED;
   if (ws && (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1))) return KDA_ERR_MISALIGNED;
@@ -160,89 +202,89 @@ Problem make_problem(const Shape& s, const KdaArgs* a, uint8_t* ws, const Layout
   P.cu = a->cu_seqlens;
   P.status = reinterpret_cast<int32_t*>(ws + L.status);
   if (s.varlen) {
-    P.chunk_idx = reinterpret_cast<const int32_t*>(ws + L.idx);
-    P.chunk_off = reinterpret_cast<const int32_t*>(ws + L.off);
-    P.nc_dev = reinterpret_cast<const int32_t*>(ws + L.nc);
+    if (a->chunk_indices) {
+      P.chunk_idx = a->chunk_indices;
+      P.chunk_off = a->chunk_offsets;
+      P.nc_dev = a->chunk_offsets + s.N;  // chunk_offsets[N] = number of chunks
+    } else if (L.idx) {
+      P.chunk_idx = reinterpret_cast<const int32_t*>(ws + L.idx);
+      P.chunk_off = reinterpret_cast<const int32_t*>(ws + L.off);
+      P.nc_dev = reinterpret_cast<const int32_t*>(ws + L.nc);
+    }
     if (L.order) P.seq_order = reinterpret_cast<const int32_t*>(ws + L.order);
   }
   return P;
 }
 
-// Shared front half of both entry points: checks, status reset, chunk table.
-// `full`: kda_chunk_fwd (needs o); otherwise kda_fwd_intra (needs its four
-// outputs).  Outputs may be NULL only when there are no tokens.
-int prologue(const KdaArgs* a, void* workspace, size_t ws_bytes, cudaStream_t st, bool full, Shape* s,
-             Layout* L) {
+// Shared front half of the entry points: checks, status reset, varlen chunk
+// metadata.  kIntra (kda_fwd_intra) needs its four outputs; the forward modes
+// need o.  Outputs may be NULL only when there are no tokens.
+int prologue(const KdaArgs* a, void* workspace, size_t ws_bytes, cudaStream_t st, Mode mode, Shape* s, Layout* L,
+             DeviceInfo* d) {
   int rc = check_shape(a, s);
   if (rc) return rc;
   if (!workspace) return KDA_ERR_INVALID;
-  if (s->BT > 0 && (full ? !a->o : (!a->Aqk || !a->Akk_inv || !a->W || !a->U))) return KDA_ERR_INVALID;
+  if (s->BT > 0 && (mode != Mode::kIntra ? !a->o : (!a->Aqk || !a->Akk_inv || !a->W || !a->U)))
+    return KDA_ERR_INVALID;
   rc = check_inputs(a, workspace, s->BT);
   if (rc) return rc;
-  *L = make_layout(*s, a, full);
+  *L = make_layout(*s, a, mode);
   if (ws_bytes < L->total) return KDA_ERR_WORKSPACE;
-  rc = check_arch();
+  rc = device_info(d);
   if (rc) return rc;
   if (!encode_fn()) return KDA_ERR_LAUNCH;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   if (cudaMemsetAsync(ws, 0, 8, st) != cudaSuccess) return KDA_ERR_LAUNCH;
   if (s->varlen && s->N > 0) {
-    if (launch_chunk_index(a->cu_seqlens, s->N, s->T, kChunk, reinterpret_cast<int32_t*>(ws + L->idx),
-                           reinterpret_cast<int32_t*>(ws + L->off), reinterpret_cast<int32_t*>(ws + L->nc),
-                           reinterpret_cast<int32_t*>(ws + L->status), st) != cudaSuccess)
-      return KDA_ERR_LAUNCH;
-    if (full && launch_seq_order(a->cu_seqlens, s->N, s->T, kChunk, reinterpret_cast<int32_t*>(ws + L->order),
-                                 st) != cudaSuccess)
+    int32_t* status = reinterpret_cast<int32_t*>(ws + L->status);
+    if (a->chunk_indices) {
+      if (launch_check_table(a->cu_seqlens, s->N, s->T, kChunk, a->chunk_indices, a->chunk_offsets, status, st) !=
+          cudaSuccess)
+        return KDA_ERR_LAUNCH;
+    } else if (mode != Mode::kFused) {
+      if (launch_chunk_index(a->cu_seqlens, s->N, s->T, kChunk, reinterpret_cast<int32_t*>(ws + L->idx),
+                             reinterpret_cast<int32_t*>(ws + L->off), reinterpret_cast<int32_t*>(ws + L->nc), status,
+                             st) != cudaSuccess)
+        return KDA_ERR_LAUNCH;
+    }
+    if (mode != Mode::kIntra &&
+        launch_seq_order(a->cu_seqlens, s->N, s->T, kChunk, reinterpret_cast<int32_t*>(ws + L->order), status,
+                         st) != cudaSuccess)
       return KDA_ERR_LAUNCH;
   }
   return KDA_OK;
 }
 
-int run_intra(const Shape& s, const KdaArgs* a, const Problem& P, const IntraOut& out, cudaStream_t st) {
-  const IntraInputs in{a->q, a->k, a->v, a->g, a->beta};
-  IntraMaps m;
+bool make_intra_maps(const Shape& s, const KdaArgs* a, IntraMaps* m) {
   const auto bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const auto none = CU_TENSOR_MAP_SWIZZLE_NONE;
-  if (!map_tokens(&m.q, a->q, bf, 2, s.K, s.Hq, s.BT, s.K, none) ||
-      !map_tokens(&m.k, a->k, bf, 2, s.K, s.Hq, s.BT, s.K, none) ||
-      !map_tokens(&m.v, a->v, bf, 2, s.V, s.Hv, s.BT, s.V, none) ||
-      !map_tokens(&m.g, a->g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, s.K, s.Hv, s.BT, s.K, none) ||
-      !map_tokens(&m.v_sw, a->v, bf, 2, s.V, s.Hv, s.BT, 64, CU_TENSOR_MAP_SWIZZLE_128B))
-    return KDA_ERR_LAUNCH;
-  return launch_intra(P, in, out, m, st) == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
+  return map_tokens(&m->q, a->q, bf, 2, s.K, s.Hq, s.BT, s.K, none) &&
+         map_tokens(&m->k, a->k, bf, 2, s.K, s.Hq, s.BT, s.K, none) &&
+         map_tokens(&m->v, a->v, bf, 2, s.V, s.Hv, s.BT, s.V, none) &&
+         map_tokens(&m->g, a->g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, s.K, s.Hv, s.BT, s.K, none) &&
+         map_tokens(&m->v_sw, a->v, bf, 2, s.V, s.Hv, s.BT, 64, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-}  // namespace
-}  // namespace kda
-
-using namespace kda;
-
-extern "C" size_t kda_workspace_size(const KdaArgs* a) {
-  Shape s;
-  if (check_shape(a, &s) != KDA_OK) return 0;
-  return make_layout(s, a, true).total;
+int run_intra(const Shape& s, const KdaArgs* a, const Problem& P, const IntraOut& out, const DeviceInfo& d,
+              cudaStream_t st) {
+  const IntraInputs in{a->q, a->k, a->v, a->g, a->beta};
+  IntraMaps m;
+  if (!make_intra_maps(s, a, &m)) return KDA_ERR_LAUNCH;
+  return launch_intra(P, in, out, m, d.dev, d.sms, st) == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
 }
 
-extern "C" int kda_chunk_fwd(const KdaArgs* a, void* workspace, size_t ws_bytes, kda_stream_t stream) {
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  Shape s;
-  Layout L;
-  int rc = prologue(a, workspace, ws_bytes, st, true, &s, &L);
-  if (rc) return rc;
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  cudaEvent_t const* ev = reinterpret_cast<cudaEvent_t const*>(a->profile_events);
-  if (ev && cudaEventRecord(ev[0], st) != cudaSuccess) return KDA_ERR_LAUNCH;
-  if (s.BT == 0 || s.nc_max == 0) {
-    // no tokens: the final state is the initial state
-    if (a->final_state) {
-      const size_t bytes = size_t(s.N) * s.Hv * s.K * s.V * 4;
-      cudaError_t e = a->initial_state
-                          ? cudaMemcpyAsync(a->final_state, a->initial_state, bytes, cudaMemcpyDeviceToDevice, st)
-                          : cudaMemsetAsync(a->final_state, 0, bytes, st);
-      if (e != cudaSuccess) return KDA_ERR_LAUNCH;
-    }
-    return KDA_OK;
-  }
+// No tokens: the final state is the initial state.
+int empty_forward(const Shape& s, const KdaArgs* a, cudaStream_t st) {
+  if (!a->final_state) return KDA_OK;
+  const size_t bytes = size_t(s.N) * s.Hv * s.K * s.V * 4;
+  const cudaError_t e = a->initial_state
+                            ? cudaMemcpyAsync(a->final_state, a->initial_state, bytes, cudaMemcpyDeviceToDevice, st)
+                            : cudaMemsetAsync(a->final_state, 0, bytes, st);
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
+}
+
+int two_pass_forward(const Shape& s, const KdaArgs* a, uint8_t* ws, const Layout& L, const DeviceInfo& d,
+                     cudaEvent_t const* ev, cudaStream_t st) {
   const Problem P = make_problem(s, a, ws, L);
   IntraOut out{};
   out.Aqk = a->Aqk;
@@ -255,10 +297,9 @@ extern "C" int kda_chunk_fwd(const KdaArgs* a, void* workspace, size_t ws_bytes,
   out.Aqk_b = ws + L.Aqk_b;
   out.Kl = ws + L.Kl;
   out.gamma = reinterpret_cast<float*>(ws + L.gamma);
-  rc = run_intra(s, a, P, out, st);
+  int rc = run_intra(s, a, P, out, d, st);
   if (rc) return rc;
   if (ev && cudaEventRecord(ev[1], st) != cudaSuccess) return KDA_ERR_LAUNCH;
-
   StateMaps m;
   const auto bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
@@ -268,17 +309,75 @@ extern "C" int kda_chunk_fwd(const KdaArgs* a, void* workspace, size_t ws_bytes,
       !map_tokens(&m.U, out.U, bf, 2, s.V, s.Hv, s.BT, s.V, CU_TENSOR_MAP_SWIZZLE_NONE) ||
       !map_tokens(&m.Kl, out.Kl, bf, 2, s.K, s.Hv, s.BT, 64, sw))
     return KDA_ERR_LAUNCH;
-  if (launch_state(P, m, out.gamma, a->initial_state, a->o, a->final_state, st) != cudaSuccess)
+  if (launch_state(P, m, out.gamma, a->initial_state, a->o, a->final_state, d.dev, st) != cudaSuccess)
     return KDA_ERR_LAUNCH;
   if (ev && cudaEventRecord(ev[2], st) != cudaSuccess) return KDA_ERR_LAUNCH;
   return KDA_OK;
+}
+
+int fused_forward(const Shape& s, const KdaArgs* a, uint8_t* ws, const Layout& L, const DeviceInfo& d,
+                  cudaEvent_t const* ev, cudaStream_t st) {
+  const Problem P = make_problem(s, a, ws, L);
+  IntraMaps m;
+  if (!make_intra_maps(s, a, &m)) return KDA_ERR_LAUNCH;
+  FusedArgs f{};
+  f.q = a->q;
+  f.k = a->k;
+  f.g = a->g;
+  f.beta = a->beta;
+  f.h0 = a->initial_state;
+  f.o = reinterpret_cast<__nv_bfloat16*>(a->o);
+  f.hT = a->final_state;
+  f.Aqk = a->Aqk;
+  f.Akk_inv = a->Akk_inv;
+  f.W = a->W;
+  f.U = a->U;
+  f.G = a->G;
+  f.QG = a->QG;
+  if (launch_fused(P, f, m, d.dev, st) != cudaSuccess) return KDA_ERR_LAUNCH;
+  if (ev && (cudaEventRecord(ev[1], st) != cudaSuccess || cudaEventRecord(ev[2], st) != cudaSuccess))
+    return KDA_ERR_LAUNCH;
+  return KDA_OK;
+}
+
+}  // namespace
+}  // namespace kda
+
+using namespace kda;
+
+extern "C" size_t kda_workspace_size(const KdaArgs* a) {
+  Shape s;
+  Mode mode;
+  if (check_shape(a, &s) != KDA_OK || forward_mode(a, &mode) != KDA_OK) return 0;
+  // the larger of the forward's and the intra primitive's needs
+  const size_t fwd = make_layout(s, a, mode).total, intra = make_layout(s, a, Mode::kIntra).total;
+  return fwd > intra ? fwd : intra;
+}
+
+extern "C" int kda_chunk_fwd(const KdaArgs* a, void* workspace, size_t ws_bytes, kda_stream_t stream) {
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (!a) return KDA_ERR_INVALID;
+  Mode mode;
+  int rc = forward_mode(a, &mode);
+  if (rc) return rc;
+  Shape s;
+  Layout L;
+  DeviceInfo d;
+  rc = prologue(a, workspace, ws_bytes, st, mode, &s, &L, &d);
+  if (rc) return rc;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cudaEvent_t const* ev = reinterpret_cast<cudaEvent_t const*>(a->profile_events);
+  if (ev && cudaEventRecord(ev[0], st) != cudaSuccess) return KDA_ERR_LAUNCH;
+  if (s.BT == 0 || s.nc_max == 0) return empty_forward(s, a, st);
+  return mode == Mode::kFused ? fused_forward(s, a, ws, L, d, ev, st) : two_pass_forward(s, a, ws, L, d, ev, st);
 }
 
 extern "C" int kda_fwd_intra(const KdaArgs* a, void* workspace, size_t ws_bytes, kda_stream_t stream) {
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   Shape s;
   Layout L;
-  int rc = prologue(a, workspace, ws_bytes, st, false, &s, &L);
+  DeviceInfo d;
+  int rc = prologue(a, workspace, ws_bytes, st, Mode::kIntra, &s, &L, &d);
   if (rc) return rc;
   if (s.BT == 0 || s.nc_max == 0) return KDA_OK;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -290,7 +389,7 @@ extern "C" int kda_fwd_intra(const KdaArgs* a, void* workspace, size_t ws_bytes,
   out.U = a->U;
   out.G = a->G;
   out.QG = a->QG;
-  return run_intra(s, a, P, out, st);
+  return run_intra(s, a, P, out, d, st);
 }
 
 extern "C" int kda_prepare_chunk_indices(const int32_t* cu_seqlens, int32_t N, int32_t T, int32_t chunk,
@@ -359,6 +458,7 @@ extern "C" const char* kda_status_string(int status) {
     case KDA_ERR_TIMEOUT: return "a bounded wait inside a kernel ran out";
     case KDA_ERR_GATE_RANGE:
       return "a chunk's cumulative log-gate fell below -KDA_MAX_CHUNK_LOG_DECAY on some channel";
+    case KDA_ERR_BAD_CHUNK_TABLE: return "the supplied chunk_indices / chunk_offsets do not match cu_seqlens";
     default: return "unknown status";
   }
 }

@@ -1,0 +1,777 @@
+// Fused chunked KDA forward: one CTA per (sequence, value head) chain runs
+// every step of the chunked form for that chain, chunk after chunk, so that
+// nothing but the inputs, the outputs and the requested intermediates crosses
+// HBM.  The intra-chunk steps of chunk c+1 (cuLA PR #131, Summary: intra-chunk
+// matrices, FP32 inverse of (I + Akk), W/U recompute) overlap the state and
+// output steps of chunk c (cuLA REPO_LAYOUT.md: chunk_delta_h.py, fwd_o.py).
+//
+// Warp roles (16 warps, 128 registers a thread):
+//   w0-w7    prep (thread = channel pair x 16-row quarter): loads of q, k, g,
+//            inclusive cumsum G, the gated operands Qg = q e^G, Kg = k e^G,
+//            Kd = k e^-G split into bf16 hi + lo, gamma = e^{G_last}.  Thread 0
+//            issues MMA1: D1 = [Qg; Kg] Kd^T with the hi/lo split (hi*hi +
+//            lo*hi, then hi*lo once Kd's low half has replaced the A operand's
+//            low half in the lo area).
+//   w8-w11   intra epilogue: Aqk rows (scale, causal mask) from D1 to the
+//            fp32 export and to a bf16 operand tile; Akk rows (beta, strict
+//            mask) to shared memory; the FP32 inverse X = (I + Akk)^-1 by
+//            16 x 16 blocks on all 128 threads; B2 = X diag(beta) as a bf16
+//            tile; the Akk_inv export; W^T from TMEM into the state pass's
+//            operand tile and the W / U exports.  w8 lane 0 issues MMA2
+//            (W^T = Kg^T B2^T, U^T = v^T B2^T), the TMA copy of each chunk's v
+//            into its operand tile and the L2 prefetch of the next chunk's
+//            q, k, v, g; a tail chunk's v rows past its end are cleared.
+//   w12-w15  state (thread = value channel v): S^T lives in TMEM in fp32 and
+//            as a bf16 copy in shared memory (the A operand).  Per chunk, w12
+//            lane 0 issues P^T = S^T W^T and O^T = S^T Qg^T, the threads form
+//            Delta^T = U^T - P^T (rows past the chunk's end zero), w12 lane 0
+//            issues S^T += Delta^T Kd and O^T += Delta^T Aqk^T, and the
+//            threads scale the state by gamma:
+//              S <- Diag(e^{G_last}) (S + Kd^T Delta)
+//                 = Diag(e^{G_last}) S + (K e^{G_last - G})^T Delta,
+//            o = scale (Qg S + (Aqk / scale) Delta).
+//
+// The bf16 hi tiles of Qg, Kg and Kd are the operands of MMA1, of MMA2 (Kg as
+// an MN-major A) and of the state MMAs (Qg, Kd), so they are written once and
+// double-buffered by chunk parity.  The lo tiles live only until MMA1 ends;
+// their area then holds the inverse's fp32 scratch.  Every wait is bounded.
+#include "kda_internal.cuh"
+
+namespace kda {
+
+namespace {
+
+constexpr int kFusedWarps = 16;
+constexpr int kFusedThreads = kFusedWarps * 32;
+constexpr int kWarpIntra0 = 8, kWarpState0 = 12;
+constexpr int kPrepThreadsF = 8 * 32;
+constexpr int kRows = 16;  // rows per prep thread
+constexpr int kLd = 68;    // fp32 row stride of the inverse's A and X tiles
+constexpr uint32_t kNbPrep = 1, kNbIntra = 2, kNbState = 3;  // named barriers
+
+// TMEM columns
+constexpr uint32_t kColD1 = 0;     // MMA1: lanes 0-63 Aqk / scale, 64-127 Akk / beta (64 cols)
+constexpr uint32_t kColW = 64;     // MMA2: W^T, lane = channel k (64 cols = tokens)
+constexpr uint32_t kColU = 128;    // MMA2: U^T, lane = channel v
+constexpr uint32_t kColP = 192;    // P^T = S^T W^T, lane = v
+constexpr uint32_t kColO = 256;    // O^T, two buffers (256, 320), lane = v
+constexpr uint32_t kColS = 384;    // S^T in fp32, lane = v, column = k
+
+__host__ __device__ constexpr uint32_t round1k(uint32_t x) { return (x + 1023u) / 1024u * 1024u; }
+
+template <int K, int V>
+struct FusedLayout {
+  static constexpr uint32_t kA1 = K * 256;  // [Qg; Kg]: K/64 atoms of 128 rows x 128 B
+  static constexpr uint32_t kB1 = K * 128;  // Kd: K/64 atoms of 64 rows x 128 B
+  static constexpr uint32_t kHi = kA1 + kB1;
+  static constexpr uint32_t kScratch = 2 * 64 * kLd * 4;  // fp32 A and X of the inverse
+  static constexpr uint32_t kLo = round1k(kA1 > kScratch ? kA1 : kScratch);
+  static constexpr uint32_t HI = 0;                        // 2 x (A1_hi, B1_hi)
+  static constexpr uint32_t LO = HI + 2 * kHi;             // A1_lo, then Kd_lo, then the inverse scratch
+  static constexpr uint32_t VT = LO + kLo;                 // v: 64 token rows, 64-channel blocks 8 KB apart
+  static constexpr uint32_t AQKB = VT + 16384;             // 2 x Aqk / scale, bf16 64 x 64, K-major
+  static constexpr uint32_t B2 = AQKB + 2 * 8192;          // X diag(beta), bf16 64 x 64, K-major
+  static constexpr uint32_t ST = B2 + 8192;                // S^T bf16: K/64 atoms of 128 rows x 128 B
+  static constexpr uint32_t WD = ST + K * 256;             // W tile (K rows of 64 tokens) / Delta^T (128 rows)
+  static constexpr uint32_t GAM = WD + 16384;              // 2 x K floats: gamma
+  static constexpr uint32_t BETA = GAM + 2 * K * 4;        // 64 floats
+  static constexpr uint32_t PART = BETA + 64 * 4;          // 2 x 4 x K floats: cumsum partial sums
+  static constexpr uint32_t BARS = PART + 2 * 4 * K * 4;
+  static constexpr int kBars = 16;
+  static constexpr uint32_t TMEM_SLOT = BARS + kBars * 8;
+  static constexpr uint32_t ABORT = TMEM_SLOT + 4;
+  static constexpr uint32_t total = ABORT + 4;
+  static constexpr uint32_t bytes = total + 1024;  // slack for the 1024-B alignment of the base
+  static_assert(LO % 1024 == 0 && VT % 1024 == 0 && AQKB % 1024 == 0 && B2 % 1024 == 0 && ST % 1024 == 0 &&
+                    WD % 1024 == 0,
+                "operand tiles must be 1024-B aligned");
+  static_assert(bytes <= 227 * 1024, "shared memory budget");
+};
+
+// barrier indices
+enum {
+  bLoA = 0,      // MMA1 hi*hi + lo*hi done: A1_lo may be overwritten            (commit)
+  bD1Full = 1,   // MMA1 done -> intra epilogue                                  (commit)
+  bD1Empty = 2,  // intra epilogue read D1 -> MMA1                               (128)
+  bLoFree = 3,   // intra epilogue done with the scratch in the lo area -> prep  (128)
+  bHiFree = 4,   // [2] state done with hi buffer b (and its gamma) -> prep, Aqk (128)
+  bVFull = 6,    // TMA: v chunk landed                                          (1 + bytes)
+  bD2Full = 7,   // MMA2 done -> intra epilogue, state                           (commit)
+  bD2Empty = 8,  // W^T / U^T read -> MMA2                                       (256)
+  bWFull = 9,    // W tile and Aqk_b written -> state MMA issue                  (128)
+  bPDone = 10,   // P^T and O^T = S^T Qg^T done -> state                         (commit)
+  bHODone = 11,  // S^T += Delta^T Kd and O^T += Delta^T Aqk^T done              (commit)
+  bDrain = 12,   // [3] final drains of the three MMA issuers                    (commit)
+};
+
+__device__ __forceinline__ uint32_t par(int n) { return uint32_t(n) & 1u; }
+
+__device__ __forceinline__ float exp2f_fast(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// x = hi + lo with hi = bf16(x), lo = bf16(x - hi), on a channel pair: stores
+// hi at hi_p, returns lo (both as bf16x2).
+__device__ __forceinline__ uint32_t split2(uint8_t* hi_p, f2 x) {
+  const uint32_t h = f2_to_bf16x2(x);
+  *reinterpret_cast<uint32_t*>(hi_p) = h;
+  return f2_to_bf16x2(f2_sub(x, f2_from_bf16x2(h)));
+}
+
+__device__ __forceinline__ uint4 pack8(const float* f) {
+  return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                    pack_bf16x2(f[6], f[7]));
+}
+
+__device__ __forceinline__ float load_beta(const void* beta, int fp32, size_t i) {
+  return fp32 ? __ldg(reinterpret_cast<const float*>(beta) + i)
+              : __bfloat162float(__ldg(reinterpret_cast<const __nv_bfloat16*>(beta) + i));
+}
+
+__device__ __forceinline__ float4 fma4(float a, float4 x, float4 acc) {
+  acc.x = fmaf(a, x.x, acc.x);
+  acc.y = fmaf(a, x.y, acc.y);
+  acc.z = fmaf(a, x.z, acc.z);
+  acc.w = fmaf(a, x.w, acc.w);
+  return acc;
+}
+
+template <int K, int V, bool kQG>
+__global__ void __launch_bounds__(kFusedThreads, 1)
+    fused_kernel(const Problem P, const FusedArgs A, const __grid_constant__ IntraMaps maps) {
+  using Lay = FusedLayout<K, V>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+  const int hv = int(blockIdx.x % unsigned(P.Hv));
+  const int n = P.varlen ? P.seq_order[blockIdx.x / unsigned(P.Hv)] : int(blockIdx.x / unsigned(P.Hv));
+  // an earlier error (bad cu_seqlens, another kernel's failure) stops the
+  // whole CTA: one thread reads the status word, so that every thread takes
+  // the same branch before the CTA's barriers
+  if (__syncthreads_or(threadIdx.x == 0 && *reinterpret_cast<volatile int32_t*>(P.status) != 0)) return;
+  int bos, len;
+  if (P.varlen) {
+    bos = P.cu[n];
+    len = P.cu[n + 1] - bos;
+  } else {
+    bos = n * P.T;
+    len = P.T;
+  }
+  const int nch = (len + kChunk - 1) / kChunk;
+  const int hq = hv / (P.Hv / P.Hq);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const size_t hrow = (size_t(n) * P.Hv + hv) * K;  // row (n, hv, k = 0) of the [N, Hv, K, V] states
+  if (nch == 0) {
+    // an empty sequence leaves its state unchanged
+    if (A.hT)
+      for (int i = tid; i < K * V; i += kFusedThreads) A.hT[hrow * V + i] = A.h0 ? A.h0[hrow * V + i] : 0.f;
+    return;
+  }
+
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + Lay::BARS);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + Lay::TMEM_SLOT);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + Lay::ABORT);
+  if (tid == 0) {
+    *abort_flag = 0;
+    mbar_init(&bar[bLoA], 1);
+    mbar_init(&bar[bD1Full], 1);
+    mbar_init(&bar[bD1Empty], 128);
+    mbar_init(&bar[bLoFree], 128);
+    mbar_init(&bar[bHiFree], 128);
+    mbar_init(&bar[bHiFree + 1], 128);
+    mbar_init(&bar[bVFull], 1);
+    mbar_init(&bar[bD2Full], 1);
+    mbar_init(&bar[bD2Empty], 256);
+    mbar_init(&bar[bWFull], 128);
+    mbar_init(&bar[bPDone], 1);
+    mbar_init(&bar[bHODone], 1);
+    for (int i = 0; i < 3; ++i) mbar_init(&bar[bDrain + i], 1);
+    fence_mbar_init();
+  }
+  if (warp == kWarpIntra0) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  constexpr uint64_t kDrainNs = 200000000ull;  // final drains: 0.2 s, whatever the abort flag says
+
+  if (warp < kWarpIntra0) {
+    // ================================================================ prep
+    const int ptid = tid;
+    const bool mma_leader = ptid == 0;  // issues MMA1
+    const int p = ptid & 63, quarter = ptid >> 6, c0 = 2 * p;
+    const bool kact = c0 < K;
+    // byte offset of this thread's channel pair in row 16*quarter of a K-major
+    // SWIZZLE_128B tile: the atom, row, 16-byte chunk and in-chunk fields are
+    // disjoint bits, so the chunk's XOR with (row % 8) is one XOR per row
+    const uint32_t cbits = ((uint32_t(c0 & 63) >> 3) << 4) | (uint32_t(c0 & 7) << 1);
+    const uint32_t rows0 = uint32_t(kRows * quarter) * 128u;
+    const uint32_t xA = uint32_t(c0 >> 6) * 16384u + rows0 + cbits;  // A1 (Qg rows 0-63, Kg rows 64-127)
+    const uint32_t xB = uint32_t(c0 >> 6) * 8192u + rows0 + cbits;   // B1 (Kd rows 0-63)
+    float* part_base = reinterpret_cast<float*>(sm + Lay::PART);
+    float* gam_base = reinterpret_cast<float*>(sm + Lay::GAM);
+    uint8_t* lo = sm + Lay::LO;
+    for (int c = 0; c < nch; ++c) {
+      const int t0 = bos + c * kChunk, L = min(kChunk, len - c * kChunk);
+      // ---- loads (all in flight together)
+      float2 g2[kRows];
+      uint32_t q2[kRows], k2[kRows];
+#pragma unroll
+      for (int rr = 0; rr < kRows; ++rr) {
+        const int i = kRows * quarter + rr;
+        g2[rr] = make_float2(0.f, 0.f);
+        q2[rr] = k2[rr] = 0u;
+        if (i < L && kact) {
+          const size_t tq = size_t(t0 + i) * P.Hq + hq, tv = size_t(t0 + i) * P.Hv + hv;
+          g2[rr] = __ldg(reinterpret_cast<const float2*>(A.g + tv * K + c0));
+          q2[rr] = __ldg(reinterpret_cast<const uint32_t*>(reinterpret_cast<const __nv_bfloat16*>(A.q) + tq * K + c0));
+          k2[rr] = __ldg(reinterpret_cast<const uint32_t*>(reinterpret_cast<const __nv_bfloat16*>(A.k) + tq * K + c0));
+        }
+      }
+      // ---- cumsum offsets across the row quarters
+      float* part = part_base + (c & 1) * 4 * K;
+      if (kact) {
+        float2 sum = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int rr = 0; rr < kRows; ++rr) {
+          sum.x += g2[rr].x;
+          sum.y += g2[rr].y;
+        }
+        *reinterpret_cast<float2*>(part + quarter * K + c0) = sum;
+      }
+      named_bar_sync(kNbPrep, kPrepThreadsF);
+      float2 G = make_float2(0.f, 0.f), glast = make_float2(0.f, 0.f);
+      if (kact) {
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq) {
+          const float2 ps = *reinterpret_cast<const float2*>(part + qq * K + c0);
+          if (qq < quarter) {
+            G.x += ps.x;
+            G.y += ps.y;
+          }
+          glast.x += ps.x;
+          glast.y += ps.y;
+        }
+      }
+      // e^{G_r - G_i} is formed as the product of q e^{G_r} and k e^{-G_i}: both
+      // stay normal fp32 numbers only while the chunk's log-decay on every
+      // channel is at most KDA_MAX_CHUNK_LOG_DECAY
+      if (kact && quarter == 0 && fminf(glast.x, glast.y) < -KDA_MAX_CHUNK_LOG_DECAY)
+        set_status(P.status, KDA_ERR_GATE_RANGE);
+      // ---- hi buffer c%2 free once the state pass is done with chunk c-2; the
+      // lo area once the inverse of chunk c-1 is done with its scratch
+      if (c >= 2) wait_bar(&bar[bHiFree + (c & 1)], par((c >> 1) - 1), abort_flag, P.status);
+      if (c >= 1) wait_bar(&bar[bLoFree], par(c - 1), abort_flag, P.status);
+      if (kact && quarter == 0)
+        *reinterpret_cast<float2*>(gam_base + (c & 1) * K + c0) = make_float2(__expf(glast.x), __expf(glast.y));
+      uint8_t* hi = sm + Lay::HI + (c & 1) * Lay::kHi;
+      uint32_t kdl[kRows];
+      if (kact) {
+        f2 G2 = f2_make(G.x, G.y);
+        const f2 kLog2e2 = f2_make(1.4426950408889634f, 1.4426950408889634f);
+#pragma unroll
+        for (int rr = 0; rr < kRows; ++rr) {
+          const int i = kRows * quarter + rr;
+          G2 = f2_add(G2, f2_make(g2[rr].x, g2[rr].y));
+          const f2 q = f2_from_bf16x2(q2[rr]);
+          const f2 k = f2_from_bf16x2(k2[rr]);
+          const float2 glv = f2_split(f2_mul(G2, kLog2e2));
+          const f2 eG = f2_make(exp2f_fast(glv.x), exp2f_fast(glv.y));
+          const f2 eN = f2_make(exp2f_fast(-glv.x), exp2f_fast(-glv.y));
+          const f2 Qg = f2_mul(q, eG);
+          const f2 Kg = f2_mul(k, eG);
+          const f2 Kd = f2_mul(k, eN);
+          const uint32_t swr = uint32_t(rr & 7) << 4, rowr = uint32_t(rr) * 128u;
+          const uint32_t oq = (xA ^ swr) + rowr, ok = oq + 8192u, od = (xB ^ swr) + rowr;
+          *reinterpret_cast<uint32_t*>(lo + oq) = split2(hi + oq, Qg);
+          *reinterpret_cast<uint32_t*>(lo + ok) = split2(hi + ok, Kg);
+          kdl[rr] = split2(hi + Lay::kA1 + od, Kd);
+          if (i < L) {
+            const size_t tok = size_t(t0 + i) * P.Hv + hv;
+            if (A.G) *reinterpret_cast<float2*>(A.G + tok * K + c0) = f2_split(G2);
+            if constexpr (kQG)
+              *reinterpret_cast<uint32_t*>(reinterpret_cast<__nv_bfloat16*>(A.QG) + tok * K + c0) = f2_to_bf16x2(Qg);
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(kNbPrep, kPrepThreadsF);
+      // ---- MMA1 (thread 0): hi*hi + lo*hi; atoms of 64 channels, A 128 rows
+      // (1024 descriptor units apart), B 64 rows (512)
+      constexpr uint32_t id = idesc_bf16_f32(128, 64);
+      const uint32_t hi_addr = smem_u32(hi), lo_addr = smem_u32(lo);
+      const uint64_t a_hi = sdesc_kmajor_sw128(hi_addr), b_hi = sdesc_kmajor_sw128(hi_addr + Lay::kA1);
+      const uint64_t lo_d = sdesc_kmajor_sw128(lo_addr);
+      if (mma_leader) {
+        if (c >= 1) wait_bar(&bar[bD1Empty], par(c - 1), abort_flag, P.status);
+        tc_fence_after();
+#pragma unroll
+        for (int at = 0; at < K / 64; ++at) umma_atom4(tmem + kColD1, a_hi + at * 1024, b_hi + at * 512, id, at > 0);
+#pragma unroll
+        for (int at = 0; at < K / 64; ++at) umma_atom4(tmem + kColD1, lo_d + at * 1024, b_hi + at * 512, id, 1);
+        umma_commit(&bar[bLoA]);
+      }
+      // ---- Kd's low half into the area A1_lo used, once hi*hi + lo*hi is done
+      wait_bar(&bar[bLoA], par(c), abort_flag, P.status);
+      if (kact) {
+#pragma unroll
+        for (int rr = 0; rr < kRows; ++rr)
+          *reinterpret_cast<uint32_t*>(lo + (xB ^ (uint32_t(rr & 7) << 4)) + uint32_t(rr) * 128u) = kdl[rr];
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(kNbPrep, kPrepThreadsF);
+      if (mma_leader) {
+        tc_fence_after();
+#pragma unroll
+        for (int at = 0; at < K / 64; ++at) umma_atom4(tmem + kColD1, a_hi + at * 1024, lo_d + at * 512, id, 1);
+        umma_commit(&bar[bD1Full]);
+      }
+    }
+    if (mma_leader) {
+      umma_commit(&bar[bDrain]);
+      mbar_wait(&bar[bDrain], 0, kDrainNs);
+    }
+
+  } else if (warp < kWarpState0) {
+    // ====================================================== intra epilogue
+    const int e = tid - kWarpIntra0 * 32;  // 0..127
+    const int q4 = warp & 3;               // TMEM lane quadrant
+    const bool akk = q4 >= 2;              // lanes 64-127: Kg rows of D1 (Akk); lanes 0-63: Qg rows (Aqk)
+    const int r = 32 * (q4 & 1) + lane;    // row of the 64 x 64 matrix
+    const bool leader = warp == kWarpIntra0 && lane == 0;
+    float* Am = reinterpret_cast<float*>(sm + Lay::LO);  // A = Akk (beta-scaled, strictly lower), fp32 64 x kLd
+    float* Xm = Am + 64 * kLd;                            // X = (I + A)^-1
+    float* sB = reinterpret_cast<float*>(sm + Lay::BETA);
+    uint8_t* wd = sm + Lay::WD;
+    uint8_t* vt = sm + Lay::VT;
+    // L2 prefetch of chunk cc's q, k, v, g (one TMA tensor prefetch each), and
+    // the TMA copy of its v rows into the v tile (64-channel boxes, SWIZZLE_128B)
+    auto prefetch = [&](int cc) {
+      const int t = bos + cc * kChunk;
+      tma_prefetch_l2_3d(&maps.q, 0, hq, t);
+      tma_prefetch_l2_3d(&maps.k, 0, hq, t);
+      tma_prefetch_l2_3d(&maps.v, 0, hv, t);
+      tma_prefetch_l2_3d(&maps.g, 0, hv, t);
+    };
+    auto load_v = [&](int cc) {
+      mbar_arrive_expect_tx(&bar[bVFull], uint32_t(V) * 64u * 2u);
+#pragma unroll
+      for (int a = 0; a < V / 64; ++a)
+        tma_load_3d(vt + a * 8192, &maps.v_sw, a * 64, hv, bos + cc * kChunk, &bar[bVFull]);
+    };
+    if (leader) {
+      prefetch(0);
+      if (nch > 1) prefetch(1);
+      load_v(0);
+    }
+    for (int c = 0; c < nch; ++c) {
+      const int t0 = bos + c * kChunk, L = min(kChunk, len - c * kChunk);
+      const float br = (akk && r < L) ? load_beta(A.beta, P.beta_fp32, size_t(t0 + r) * P.Hv + hv) : 0.f;
+      wait_bar(&bar[bD1Full], par(c), abort_flag, P.status);
+      tc_fence_after();
+      {
+        uint32_t xa[32], xb[32];
+        tmem_ld_x32(tmem_addr(tmem, 32 * q4, kColD1), xa);
+        tmem_ld_x32(tmem_addr(tmem, 32 * q4, kColD1 + 32), xb);
+        tc_fence_before();
+        mbar_arrive(&bar[bD1Empty]);
+        if (akk) {
+          // row r of A: beta_r Akk[r][i] for i < r, zero elsewhere
+          float* arow = Am + r * kLd;
+#pragma unroll
+          for (int i = 0; i < 64; i += 4) {
+            float a4[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              a4[j] = (i + j < r) ? br * __uint_as_float(i + j < 32 ? xa[i + j] : xb[i + j - 32]) : 0.f;
+            *reinterpret_cast<float4*>(arow + i) = make_float4(a4[0], a4[1], a4[2], a4[3]);
+          }
+          sB[r] = br;
+        } else {
+          // Aqk row r (causal mask): bf16 operand tile of O^T += Delta^T Aqk^T
+          // (without scale: the state pass multiplies O by scale at the end)
+          // and the fp32 export with scale; the tile of chunk c-2 must be done
+          if (c >= 2) wait_bar(&bar[bHiFree + (c & 1)], par((c >> 1) - 1), abort_flag, P.status);
+          uint8_t* aqkb = sm + Lay::AQKB + (c & 1) * 8192;
+          float* arow = A.Aqk ? A.Aqk + (size_t(t0 + r) * P.Hv + hv) * 64 : nullptr;
+#pragma unroll
+          for (int i = 0; i < 64; i += 8) {
+            float f[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) f[j] = (i + j <= r) ? __uint_as_float(i + j < 32 ? xa[i + j] : xb[i + j - 32]) : 0.f;
+            *reinterpret_cast<uint4*>(aqkb + sw128_offset(uint32_t(r), uint32_t(i), 64)) = pack8(f);
+            if (arow && r < L) {
+              *reinterpret_cast<float4*>(arow + i) =
+                  make_float4(P.scale * f[0], P.scale * f[1], P.scale * f[2], P.scale * f[3]);
+              *reinterpret_cast<float4*>(arow + i + 4) =
+                  make_float4(P.scale * f[4], P.scale * f[5], P.scale * f[6], P.scale * f[7]);
+            }
+          }
+          fence_proxy_async_smem();
+        }
+      }
+      named_bar_sync(kNbIntra, 128);
+      // ---- X = (I + A)^-1 by 16 x 16 blocks.  Diagonal blocks: forward
+      // substitution, thread = (block d, column cc), on the threads that wrote A.
+      if (akk) {
+        const int d = (e - 64) >> 4, cc = e & 15, base = 16 * d;
+        float x[16];
+#pragma unroll
+        for (int rr = 0; rr < 16; ++rr) {
+          float acc = 0.f;
+#pragma unroll
+          for (int i = 0; i < rr; ++i) acc = fmaf(Am[(base + rr) * kLd + base + i], x[i], acc);
+          x[rr] = (rr == cc ? 1.f : 0.f) - acc;
+        }
+#pragma unroll
+        for (int rr = 0; rr < 16; ++rr) Xm[(base + rr) * kLd + base + cc] = x[rr];
+      }
+      named_bar_sync(kNbIntra, 128);
+      // 32 x 32 diagonal blocks: X_10 = -X_11 (A_10 X_00) and X_32 = -X_33 (A_32 X_22).
+      // Thread = (half b, row, column quad); T goes into the dead block A_00 / A_22.
+      {
+        const int b = e >> 6, row = (e >> 2) & 15, c4 = 4 * (e & 3);
+        const int ro = b ? 48 : 16, co = b ? 32 : 0;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+        for (int kk = c4; kk < 16; ++kk)
+          acc = fma4(Am[(ro + row) * kLd + co + kk], *reinterpret_cast<const float4*>(Xm + (co + kk) * kLd + co + c4), acc);
+        *reinterpret_cast<float4*>(Am + (co + row) * kLd + co + c4) = acc;
+        named_bar_sync(kNbIntra, 128);
+        float4 xs = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+        for (int m = 0; m <= row; ++m)
+          xs = fma4(Xm[(ro + row) * kLd + ro + m], *reinterpret_cast<const float4*>(Am + (co + m) * kLd + co + c4), xs);
+        *reinterpret_cast<float4*>(Xm + (ro + row) * kLd + co + c4) = make_float4(-xs.x, -xs.y, -xs.z, -xs.w);
+      }
+      named_bar_sync(kNbIntra, 128);
+      // the lower-left 32 x 32 block: X_BL = -X_BR (A_BL X_TL).  Thread = (row,
+      // column octet); T goes into the dead top-left block of A.
+      {
+        const int row = e >> 2, c8 = 8 * (e & 3);
+        float4 t0v = make_float4(0.f, 0.f, 0.f, 0.f), t1v = t0v;
+#pragma unroll 4
+        for (int kk = c8; kk < 32; ++kk) {
+          const float a = Am[(32 + row) * kLd + kk];
+          t0v = fma4(a, *reinterpret_cast<const float4*>(Xm + kk * kLd + c8), t0v);
+          t1v = fma4(a, *reinterpret_cast<const float4*>(Xm + kk * kLd + c8 + 4), t1v);
+        }
+        *reinterpret_cast<float4*>(Am + row * kLd + c8) = t0v;
+        *reinterpret_cast<float4*>(Am + row * kLd + c8 + 4) = t1v;
+        named_bar_sync(kNbIntra, 128);
+        float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
+#pragma unroll 4
+        for (int m = 0; m <= row; ++m) {
+          const float xv = Xm[(32 + row) * kLd + 32 + m];
+          x0 = fma4(xv, *reinterpret_cast<const float4*>(Am + m * kLd + c8), x0);
+          x1 = fma4(xv, *reinterpret_cast<const float4*>(Am + m * kLd + c8 + 4), x1);
+        }
+        *reinterpret_cast<float4*>(Xm + (32 + row) * kLd + c8) = make_float4(-x0.x, -x0.y, -x0.z, -x0.w);
+        *reinterpret_cast<float4*>(Xm + (32 + row) * kLd + c8 + 4) = make_float4(-x1.x, -x1.y, -x1.z, -x1.w);
+      }
+      named_bar_sync(kNbIntra, 128);
+      // ---- v of this chunk: a tail chunk's rows past its end hold tokens of
+      // the next chunk or sequence; clear them so that U depends on this
+      // chunk's tokens alone
+      wait_bar(&bar[bVFull], par(c), abort_flag, P.status);
+      if (L < kChunk) {
+        const int pieces = (kChunk - L) * 8;  // 16-byte pieces per 64-channel block
+        for (int a = 0; a < V / 64; ++a)
+          for (int i = e; i < pieces; i += 128)
+            *reinterpret_cast<uint4*>(vt + a * 8192 + (L + (i >> 3)) * 128 + (i & 7) * 16) = make_uint4(0, 0, 0, 0);
+      }
+      // ---- B2 = X diag(beta) (bf16, K-major rows r); B2 of chunk c-1 was read
+      // by MMA2(c-1), whose completion these threads saw before its W tile
+      {
+        const int rr = e >> 1, c32 = 32 * (e & 1);
+        uint8_t* b2 = sm + Lay::B2;
+#pragma unroll
+        for (int j = 0; j < 32; j += 8) {
+          const int col = c32 + j;
+          float f[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) f[i] = (col + i <= rr) ? Xm[rr * kLd + col + i] * sB[col + i] : 0.f;
+          *reinterpret_cast<uint4*>(b2 + sw128_offset(uint32_t(rr), uint32_t(col), 64)) = pack8(f);
+        }
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(kNbIntra, 128);
+      if (leader) {
+        // MMA2: W^T = Kg^T B2^T, U^T = v^T B2^T (M = 128 channels, N = 64, K = 64
+        // tokens).  Kg is read in place from the Kg rows of A1_hi as an MN-major
+        // operand (the next 64 channels one A1 atom, 16 KB, further on); v from
+        // its TMA tile (64-channel blocks 8 KB apart).  A K step of 16 tokens is
+        // 2048 B on the A side, 32 B on B2.
+        if (c >= 1) wait_bar(&bar[bD2Empty], par(c - 1), abort_flag, P.status);
+        tc_fence_after();
+        constexpr uint32_t idmn = idesc_bf16_f32(128, 64) | kIdescAMajorMN;
+        const uint32_t hi_addr = smem_u32(sm + Lay::HI + (c & 1) * Lay::kHi);
+        const uint64_t a_kg = sdesc_mnmajor_sw128(hi_addr + 8192, 16384);
+        const uint64_t a_v = sdesc_mnmajor_sw128(smem_u32(sm + Lay::VT), 8192);
+        const uint64_t b2 = sdesc_kmajor_sw128(smem_u32(sm + Lay::B2));
+        umma_k4(tmem + kColW, a_kg, b2, idmn, 0, 2048 / 16, 2);
+        umma_k4(tmem + kColU, a_v, b2, idmn, 0, 2048 / 16, 2);
+        umma_commit(&bar[bD2Full]);
+      }
+      __syncwarp();
+      // ---- Akk_inv export by whole rows (8 passes of 8 rows x 16 column quads)
+      if (A.Akk_inv) {
+#pragma unroll 2
+        for (int it = 0; it < 8; ++it) {
+          const int row = 8 * it + (e >> 4), c4 = 4 * (e & 15);
+          if (row < L) {
+            const float4 xv = *reinterpret_cast<const float4*>(Xm + row * kLd + c4);
+            const float4 o4 = make_float4(c4 <= row ? xv.x : 0.f, c4 + 1 <= row ? xv.y : 0.f,
+                                          c4 + 2 <= row ? xv.z : 0.f, c4 + 3 <= row ? xv.w : 0.f);
+            *reinterpret_cast<float4*>(A.Akk_inv + (size_t(t0 + row) * P.Hv + hv) * 64 + c4) = o4;
+          }
+        }
+      }
+      mbar_arrive(&bar[bLoFree]);
+      // ---- W^T (lane = channel k) into the W tile of the state pass (MN-major:
+      // row k holds its 64 tokens) and the W / U exports (thread = channel)
+      wait_bar(&bar[bD2Full], par(c), abort_flag, P.status);
+      if (leader) {
+        // MMA2 is done with the v tile: copy the next chunk's v, prefetch the one after
+        if (c + 1 < nch) load_v(c + 1);
+        if (c + 2 < nch) prefetch(c + 2);
+      }
+      if (c >= 1) wait_bar(&bar[bHODone], par(c - 1), abort_flag, P.status);  // Delta^T(c-1) consumed
+      tc_fence_after();
+      {
+        const int ch = 32 * q4 + lane;
+        uint32_t w[32];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          tmem_ld_x32(tmem_addr(tmem, 32 * q4, kColW + 32 * h), w);
+          if (ch < K) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              float f[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(w[8 * j + i]);
+              *reinterpret_cast<uint4*>(wd + ch * 128 + ((uint32_t(4 * h + j) ^ uint32_t(ch & 7)) << 4)) = pack8(f);
+            }
+            if (A.W) {
+              __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(A.W) + (size_t(t0 + 32 * h) * P.Hv + hv) * K + ch;
+#pragma unroll
+              for (int t = 0; t < 32; ++t)
+                if (32 * h + t < L) dst[size_t(t) * P.Hv * K] = __float2bfloat16_rn(__uint_as_float(w[t]));
+            }
+          }
+        }
+        if (A.U) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            tmem_ld_x32(tmem_addr(tmem, 32 * q4, kColU + 32 * h), w);
+            if (ch < V) {
+              __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(A.U) + (size_t(t0 + 32 * h) * P.Hv + hv) * V + ch;
+#pragma unroll
+              for (int t = 0; t < 32; ++t)
+                if (32 * h + t < L) dst[size_t(t) * P.Hv * V] = __float2bfloat16_rn(__uint_as_float(w[t]));
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&bar[bD2Empty]);
+      fence_proxy_async_smem();
+      mbar_arrive(&bar[bWFull]);
+    }
+    if (leader) {
+      // after an abort: the last v copy and the last MMA2 must land before exit
+      mbar_wait(&bar[bVFull], par(nch - 1), kDrainNs);
+      umma_commit(&bar[bDrain + 1]);
+      mbar_wait(&bar[bDrain + 1], 0, kDrainNs);
+    }
+
+  } else {
+    // =============================================================== state
+    const int q4 = warp & 3;
+    const int v = 32 * q4 + lane;  // value channel = TMEM lane
+    const bool vv = v < V;
+    const bool leader = warp == kWarpState0 && lane == 0;
+    uint8_t* st = sm + Lay::ST;
+    uint8_t* wd = sm + Lay::WD;
+    const float* gam_base = reinterpret_cast<const float*>(sm + Lay::GAM);
+    const uint32_t lane_base = tmem_addr(tmem, 32 * q4, 0);
+    // row v of the bf16 S^T tile, columns j .. j + 31
+    auto store_st = [&](int j, const uint32_t (&s)[32]) {
+#pragma unroll
+      for (int i = 0; i < 32; i += 8) {
+        float f[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) f[u] = __uint_as_float(s[i + u]);
+        *reinterpret_cast<uint4*>(st + sw128_offset(uint32_t(v), uint32_t(j + i), 128)) = pack8(f);
+      }
+    };
+    // O of chunk cc (TMEM buffer cc % 2) to o, scaled
+    auto read_o = [&](int cc) {
+      const int t0 = bos + cc * kChunk, L = min(kChunk, len - cc * kChunk);
+      uint32_t o[32];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        tmem_ld_x32(lane_base + kColO + 64 * (cc & 1) + 32 * h, o);
+        if (vv) {
+          __nv_bfloat16* dst = A.o + (size_t(t0 + 32 * h) * P.Hv + hv) * V + v;
+#pragma unroll
+          for (int t = 0; t < 32; ++t)
+            if (32 * h + t < L) dst[size_t(t) * P.Hv * V] = __float2bfloat16_rn(P.scale * __uint_as_float(o[t]));
+        }
+      }
+    };
+    // initial state into TMEM (fp32) and the bf16 A operand
+#pragma unroll 1
+    for (int j = 0; j < K; j += 32) {
+      uint32_t s[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) s[i] = __float_as_uint((A.h0 && vv) ? A.h0[(hrow + j + i) * V + v] : 0.f);
+      tmem_st_x32(lane_base + kColS + j, s);
+      store_st(j, s);
+    }
+    tmem_st_wait();
+    fence_proxy_async_smem();
+    tc_fence_before();
+    named_bar_sync(kNbState, 128);
+    for (int c = 0; c < nch; ++c) {
+      const int L = min(kChunk, len - c * kChunk);
+      const uint32_t hi_addr = smem_u32(sm + Lay::HI + (c & 1) * Lay::kHi);
+      const uint32_t ocol = kColO + 64 * (c & 1);
+      if (leader) {
+        // P^T = S^T W^T (W tile MN-major: a K step of 16 channels is 2048 B), then
+        // O^T = S^T Qg^T (Qg rows 0-63 of A1_hi, K-major)
+        wait_bar(&bar[bWFull], par(c), abort_flag, P.status);
+        tc_fence_after();
+        constexpr uint32_t idP = idesc_bf16_f32(128, 64) | kIdescBMajorMN;
+        constexpr uint32_t id64 = idesc_bf16_f32(128, 64);
+        const uint64_t a_st = sdesc_kmajor_sw128(smem_u32(st));
+        const uint64_t b_w = sdesc_mnmajor_sw128(smem_u32(wd), 8192);
+        const uint64_t b_qg = sdesc_kmajor_sw128(hi_addr);
+#pragma unroll
+        for (int g = 0; g < K / 64; ++g) umma_k4(tmem + kColP, a_st + g * 1024, b_w + g * 512, idP, g > 0, 2, 128);
+        umma_commit(&bar[bPDone]);
+#pragma unroll
+        for (int g = 0; g < K / 64; ++g) umma_atom4(tmem + ocol, a_st + g * 1024, b_qg + g * 1024, id64, g > 0);
+      }
+      __syncwarp();
+      if (c >= 1) read_o(c - 1);
+      wait_bar(&bar[bD2Full], par(c), abort_flag, P.status);
+      wait_bar(&bar[bPDone], par(c), abort_flag, P.status);
+      tc_fence_after();
+      // Delta^T row v: U^T - P^T, tokens past the chunk's end zero (into the W
+      // tile's area: P, its only reader, is done)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t pr[32], ur[32];
+        tmem_ld_x32(lane_base + kColP + 32 * h, pr);
+        tmem_ld_x32(lane_base + kColU + 32 * h, ur);
+#pragma unroll
+        for (int j = 0; j < 32; j += 8) {
+          float d[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            d[i] = (vv && 32 * h + j + i < L) ? __uint_as_float(ur[j + i]) - __uint_as_float(pr[j + i]) : 0.f;
+          *reinterpret_cast<uint4*>(wd + v * 128 + ((uint32_t((32 * h + j) >> 3) ^ uint32_t(v & 7)) << 4)) = pack8(d);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&bar[bD2Empty]);
+      fence_proxy_async_smem();
+      named_bar_sync(kNbState, 128);
+      if (leader) {
+        // S^T += Delta^T Kd (Kd token rows of B1_hi as an MN-major B: 64-channel
+        // blocks 8 KB apart, a K step of 16 tokens 2048 B), O^T += Delta^T Aqk^T
+        tc_fence_after();
+        constexpr uint32_t idH = idesc_bf16_f32(128, K) | kIdescBMajorMN;
+        constexpr uint32_t id64 = idesc_bf16_f32(128, 64);
+        const uint64_t a_d = sdesc_kmajor_sw128(smem_u32(wd));
+        const uint64_t b_kd = sdesc_mnmajor_sw128(hi_addr + Lay::kA1, 8192);
+        const uint64_t b_aqk = sdesc_kmajor_sw128(smem_u32(sm + Lay::AQKB + (c & 1) * 8192));
+        umma_k4(tmem + kColS, a_d, b_kd, idH, 1, 2, 2048 / 16);
+        umma_atom4(tmem + ocol, a_d, b_aqk, id64, 1);
+        umma_commit(&bar[bHODone]);
+      }
+      __syncwarp();
+      wait_bar(&bar[bHODone], par(c), abort_flag, P.status);
+      tc_fence_after();
+      // S <- gamma * (S + Kd^T Delta), in TMEM and as the bf16 A operand
+      const float* gm = gam_base + (c & 1) * K;
+#pragma unroll 1
+      for (int j = 0; j < K; j += 32) {
+        uint32_t s[32];
+        tmem_ld_x32(lane_base + kColS + j, s);
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+          const float4 g4 = *reinterpret_cast<const float4*>(gm + j + i);
+          s[i] = __float_as_uint(__uint_as_float(s[i]) * g4.x);
+          s[i + 1] = __float_as_uint(__uint_as_float(s[i + 1]) * g4.y);
+          s[i + 2] = __float_as_uint(__uint_as_float(s[i + 2]) * g4.z);
+          s[i + 3] = __float_as_uint(__uint_as_float(s[i + 3]) * g4.w);
+        }
+        tmem_st_x32(lane_base + kColS + j, s);
+        store_st(j, s);
+      }
+      tmem_st_wait();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&bar[bHiFree + (c & 1)]);
+      named_bar_sync(kNbState, 128);
+    }
+    read_o(nch - 1);
+    if (A.hT) {
+#pragma unroll 1
+      for (int j = 0; j < K; j += 32) {
+        uint32_t s[32];
+        tmem_ld_x32(lane_base + kColS + j, s);
+        if (vv)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) A.hT[(hrow + j + i) * V + v] = __uint_as_float(s[i]);
+      }
+    }
+    if (leader) {
+      umma_commit(&bar[bDrain + 2]);
+      mbar_wait(&bar[bDrain + 2], 0, kDrainNs);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpIntra0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int K, int V, bool kQG>
+cudaError_t launch_fused_t(const Problem& P, const FusedArgs& A, const IntraMaps& maps, int dev, cudaStream_t s) {
+  constexpr uint32_t smem = FusedLayout<K, V>::bytes;
+  cudaError_t e = set_smem_once<fused_kernel<K, V, kQG>>(smem, dev);
+  if (e != cudaSuccess) return e;
+  const long long grid = (long long)P.N * P.Hv;
+  if (grid <= 0) return cudaSuccess;
+  fused_kernel<K, V, kQG><<<unsigned(grid), kFusedThreads, smem, s>>>(P, A, maps);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fused(const Problem& P, const FusedArgs& A, const IntraMaps& maps, int dev, cudaStream_t s) {
+  // The optional QG export has its own instantiations, so that the usual
+  // prep loop carries none of its code.
+  const bool qg = A.QG != nullptr;
+  if (P.K == 128 && P.V == 128)
+    return qg ? launch_fused_t<128, 128, true>(P, A, maps, dev, s) : launch_fused_t<128, 128, false>(P, A, maps, dev, s);
+  if (P.K == 128 && P.V == 64)
+    return qg ? launch_fused_t<128, 64, true>(P, A, maps, dev, s) : launch_fused_t<128, 64, false>(P, A, maps, dev, s);
+  if (P.K == 64 && P.V == 128)
+    return qg ? launch_fused_t<64, 128, true>(P, A, maps, dev, s) : launch_fused_t<64, 128, false>(P, A, maps, dev, s);
+  if (P.K == 64 && P.V == 64)
+    return qg ? launch_fused_t<64, 64, true>(P, A, maps, dev, s) : launch_fused_t<64, 64, false>(P, A, maps, dev, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace kda

@@ -1,6 +1,7 @@
 // Internal declarations shared by the host API and the kernels.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -12,6 +13,7 @@ namespace kda {
 
 constexpr int kChunk = 64;                          // rows per chunk
 constexpr uint64_t kWaitLimitNs = 2000000000ull;    // bounded waits: 2 s
+constexpr int kMaxDevicesCached = 64;               // per-device caches of launch attributes
 
 // Sizes and chunk bookkeeping of one call, passed by value to every kernel.
 struct Problem {
@@ -89,6 +91,22 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
   }
 }
 
+// A kernel's dynamic shared memory attribute, set once per device (`dev` is
+// the current device).  The cache belongs to the kernel itself (a template
+// parameter), not to its type: instantiations of one kernel template share a
+// type but each needs its own attribute.  It is per process and does not
+// survive a cudaDeviceReset, after which the attribute would have to be set
+// again.
+template <auto* Kern>
+cudaError_t set_smem_once(uint32_t bytes, int dev) {
+  static std::atomic<uint32_t> done[kMaxDevicesCached];
+  if (dev >= 0 && dev < kMaxDevicesCached && done[dev].load(std::memory_order_acquire) == bytes)
+    return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes));
+  if (e == cudaSuccess && dev >= 0 && dev < kMaxDevicesCached) done[dev].store(bytes, std::memory_order_release);
+  return e;
+}
+
 // ---- host-side launchers (defined next to their kernels) ----
 struct IntraOut {
   float* Aqk;       // fp32 [BT, Hv, 64] (may be null)
@@ -121,12 +139,33 @@ struct StateMaps {
   CUtensorMap W, Qs, Aqk_b, U, Kl;
 };
 
+// Pointers of the fused forward (one kernel for the whole path).
+struct FusedArgs {
+  const void* q;            // bf16 [BT, Hq, K]
+  const void* k;            // bf16 [BT, Hq, K]
+  const float* g;           // fp32 [BT, Hv, K]
+  const void* beta;         // bf16 or fp32 [BT, Hv]
+  const float* h0;          // fp32 [N, Hv, K, V] or null (zeros)
+  __nv_bfloat16* o;         // bf16 [BT, Hv, V]
+  float* hT;                // fp32 [N, Hv, K, V] or null
+  float* Aqk;               // fp32 [BT, Hv, 64] or null
+  float* Akk_inv;           // fp32 [BT, Hv, 64] or null
+  void* W;                  // bf16 [BT, Hv, K] or null
+  void* U;                  // bf16 [BT, Hv, V] or null
+  float* G;                 // fp32 [BT, Hv, K] or null
+  void* QG;                 // bf16 [BT, Hv, K] or null
+};
+
 cudaError_t launch_chunk_index(const int32_t* cu, int N, int T, int chunk, int32_t* idx, int32_t* off,
                                int32_t* nc, int32_t* status, cudaStream_t s);
-cudaError_t launch_seq_order(const int32_t* cu, int N, int T, int chunk, int32_t* order, cudaStream_t s);
+cudaError_t launch_check_table(const int32_t* cu, int N, int T, int chunk, const int32_t* idx, const int32_t* off,
+                               int32_t* status, cudaStream_t s);
+cudaError_t launch_seq_order(const int32_t* cu, int N, int T, int chunk, int32_t* order, int32_t* status,
+                             cudaStream_t s);
 cudaError_t launch_intra(const Problem& P, const IntraInputs& in, const IntraOut& out, const IntraMaps& maps,
-                         cudaStream_t s);
+                         int dev, int sms, cudaStream_t s);
 cudaError_t launch_state(const Problem& P, const StateMaps& maps, const float* gamma, const float* h0,
-                         void* o, float* hT, cudaStream_t s);
+                         void* o, float* hT, int dev, cudaStream_t s);
+cudaError_t launch_fused(const Problem& P, const FusedArgs& A, const IntraMaps& maps, int dev, cudaStream_t s);
 
 }  // namespace kda

@@ -144,7 +144,10 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
   using Lay = IntraLayout<K, V>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  if (*reinterpret_cast<volatile int32_t*>(P.status) != 0) return;
+  // an earlier error (bad cu_seqlens, another kernel's failure) stops the
+  // whole CTA: one thread reads the status word, so that every thread takes
+  // the same branch before the CTA's barriers
+  if (__syncthreads_or(threadIdx.x == 0 && *reinterpret_cast<volatile int32_t*>(P.status) != 0)) return;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + Lay::bars);
@@ -705,16 +708,12 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
 
 template <int K, int V, bool kQG, bool kTF32>
 cudaError_t launch_intra_t(const Problem& P, const IntraInputs& in, const IntraOut& out, const IntraMaps& maps,
-                           cudaStream_t s) {
+                           int dev, int sms, cudaStream_t s) {
   constexpr uint32_t smem = IntraLayout<K, V>::bytes;
-  cudaError_t e =
-      cudaFuncSetAttribute(intra_kernel<K, V, kQG, kTF32>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = set_smem_once<intra_kernel<K, V, kQG, kTF32>>(smem, dev);
   if (e != cudaSuccess) return e;
   const long long items = (long long)P.nc_max * P.Hv;
   if (items <= 0) return cudaSuccess;
-  int dev = 0, sms = 0;
-  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   const unsigned grid = unsigned(items < sms ? items : sms);
   intra_kernel<K, V, kQG, kTF32><<<grid, kIntraThreads, smem, s>>>(P, in.q, in.k, in.v, in.g, in.beta, out, maps);
   return cudaGetLastError();
@@ -723,7 +722,7 @@ cudaError_t launch_intra_t(const Problem& P, const IntraInputs& in, const IntraO
 }  // namespace
 
 cudaError_t launch_intra(const Problem& P, const IntraInputs& in, const IntraOut& out, const IntraMaps& maps,
-                         cudaStream_t s) {
+                         int dev, int sms, cudaStream_t s) {
   // The optional QG export has its own instantiations: any code added to the
   // prep's row loop changes its register allocation, so the usual path
   // carries none of it.
@@ -731,31 +730,31 @@ cudaError_t launch_intra(const Problem& P, const IntraInputs& in, const IntraOut
   const bool qg = out.QG != nullptr;
   if (P.tf32) {
     if (P.K == 128 && P.V == 128)
-      return qg ? launch_intra_t<128, 128, true, true>(P, in, out, maps, s)
-                : launch_intra_t<128, 128, false, true>(P, in, out, maps, s);
+      return qg ? launch_intra_t<128, 128, true, true>(P, in, out, maps, dev, sms, s)
+                : launch_intra_t<128, 128, false, true>(P, in, out, maps, dev, sms, s);
     if (P.K == 128 && P.V == 64)
-      return qg ? launch_intra_t<128, 64, true, true>(P, in, out, maps, s)
-                : launch_intra_t<128, 64, false, true>(P, in, out, maps, s);
+      return qg ? launch_intra_t<128, 64, true, true>(P, in, out, maps, dev, sms, s)
+                : launch_intra_t<128, 64, false, true>(P, in, out, maps, dev, sms, s);
     if (P.K == 64 && P.V == 128)
-      return qg ? launch_intra_t<64, 128, true, true>(P, in, out, maps, s)
-                : launch_intra_t<64, 128, false, true>(P, in, out, maps, s);
+      return qg ? launch_intra_t<64, 128, true, true>(P, in, out, maps, dev, sms, s)
+                : launch_intra_t<64, 128, false, true>(P, in, out, maps, dev, sms, s);
     if (P.K == 64 && P.V == 64)
-      return qg ? launch_intra_t<64, 64, true, true>(P, in, out, maps, s)
-                : launch_intra_t<64, 64, false, true>(P, in, out, maps, s);
+      return qg ? launch_intra_t<64, 64, true, true>(P, in, out, maps, dev, sms, s)
+                : launch_intra_t<64, 64, false, true>(P, in, out, maps, dev, sms, s);
     return cudaErrorInvalidValue;
   }
   if (P.K == 128 && P.V == 128)
-    return qg ? launch_intra_t<128, 128, true, false>(P, in, out, maps, s)
-              : launch_intra_t<128, 128, false, false>(P, in, out, maps, s);
+    return qg ? launch_intra_t<128, 128, true, false>(P, in, out, maps, dev, sms, s)
+              : launch_intra_t<128, 128, false, false>(P, in, out, maps, dev, sms, s);
   if (P.K == 128 && P.V == 64)
-    return qg ? launch_intra_t<128, 64, true, false>(P, in, out, maps, s)
-              : launch_intra_t<128, 64, false, false>(P, in, out, maps, s);
+    return qg ? launch_intra_t<128, 64, true, false>(P, in, out, maps, dev, sms, s)
+              : launch_intra_t<128, 64, false, false>(P, in, out, maps, dev, sms, s);
   if (P.K == 64 && P.V == 128)
-    return qg ? launch_intra_t<64, 128, true, false>(P, in, out, maps, s)
-              : launch_intra_t<64, 128, false, false>(P, in, out, maps, s);
+    return qg ? launch_intra_t<64, 128, true, false>(P, in, out, maps, dev, sms, s)
+              : launch_intra_t<64, 128, false, false>(P, in, out, maps, dev, sms, s);
   if (P.K == 64 && P.V == 64)
-    return qg ? launch_intra_t<64, 64, true, false>(P, in, out, maps, s)
-              : launch_intra_t<64, 64, false, false>(P, in, out, maps, s);
+    return qg ? launch_intra_t<64, 64, true, false>(P, in, out, maps, dev, sms, s)
+              : launch_intra_t<64, 64, false, false>(P, in, out, maps, dev, sms, s);
   return cudaErrorInvalidValue;
 }
 

@@ -95,7 +95,10 @@ __global__ void __launch_bounds__(kStateThreads, 1)
 
   const int hv = blockIdx.x % P.Hv;
   const int n = P.varlen ? P.seq_order[blockIdx.x / P.Hv] : blockIdx.x / P.Hv;  // longest chains first
-  if (*reinterpret_cast<volatile int32_t*>(P.status) != 0) return;
+  // an earlier error (bad cu_seqlens, another kernel's failure) stops the
+  // whole CTA: one thread reads the status word, so that every thread takes
+  // the same branch before the CTA's barriers
+  if (__syncthreads_or(threadIdx.x == 0 && *reinterpret_cast<volatile int32_t*>(P.status) != 0)) return;
   int bos, len, gc0;
   if (P.varlen) {
     bos = P.cu[n];
@@ -341,9 +344,9 @@ __global__ void __launch_bounds__(kStateThreads, 1)
 
 template <int K, int V>
 cudaError_t launch_state_t(const Problem& P, const StateMaps& maps, const float* gamma, const float* h0, void* o,
-                           float* hT, cudaStream_t s) {
+                           float* hT, int dev, cudaStream_t s) {
   constexpr uint32_t smem = StateLayout<K, V>::bytes;
-  cudaError_t e = cudaFuncSetAttribute(state_kernel<K, V>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = set_smem_once<state_kernel<K, V>>(smem, dev);
   if (e != cudaSuccess) return e;
   const long long grid = (long long)P.N * P.Hv;
   if (grid <= 0) return cudaSuccess;
@@ -355,11 +358,11 @@ cudaError_t launch_state_t(const Problem& P, const StateMaps& maps, const float*
 }  // namespace
 
 cudaError_t launch_state(const Problem& P, const StateMaps& maps, const float* gamma, const float* h0, void* o,
-                         float* hT, cudaStream_t s) {
-  if (P.K == 128 && P.V == 128) return launch_state_t<128, 128>(P, maps, gamma, h0, o, hT, s);
-  if (P.K == 128 && P.V == 64) return launch_state_t<128, 64>(P, maps, gamma, h0, o, hT, s);
-  if (P.K == 64 && P.V == 128) return launch_state_t<64, 128>(P, maps, gamma, h0, o, hT, s);
-  if (P.K == 64 && P.V == 64) return launch_state_t<64, 64>(P, maps, gamma, h0, o, hT, s);
+                         float* hT, int dev, cudaStream_t s) {
+  if (P.K == 128 && P.V == 128) return launch_state_t<128, 128>(P, maps, gamma, h0, o, hT, dev, s);
+  if (P.K == 128 && P.V == 64) return launch_state_t<128, 64>(P, maps, gamma, h0, o, hT, dev, s);
+  if (P.K == 64 && P.V == 128) return launch_state_t<64, 128>(P, maps, gamma, h0, o, hT, dev, s);
+  if (P.K == 64 && P.V == 64) return launch_state_t<64, 64>(P, maps, gamma, h0, o, hT, dev, s);
   return cudaErrorInvalidValue;
 }
 

@@ -27,6 +27,15 @@ def _check_inputs(q, k, v, g, beta, cu_seqlens, initial_state):
     for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta)):
         if not isinstance(t, torch.Tensor) or not t.is_cuda:
             raise ValueError(f"{name} must be a CUDA tensor")
+    dev = q.device
+    for name, t in (("k", k), ("v", v), ("g", g), ("beta", beta), ("cu_seqlens", cu_seqlens),
+                    ("initial_state", initial_state)):
+        if t is None:
+            continue
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if t.device != dev:
+            raise ValueError(f"{name} is on {t.device}, q on {dev}: all tensors must be on one device")
     if q.dtype != torch.bfloat16 or k.dtype != torch.bfloat16 or v.dtype != torch.bfloat16:
         raise ValueError("q, k, v must be bfloat16")
     if g.dtype != torch.float32:
@@ -40,7 +49,7 @@ def _check_inputs(q, k, v, g, beta, cu_seqlens, initial_state):
     if v.shape[:2] != (B, T) or tuple(g.shape) != (B, T, Hv, K) or tuple(beta.shape) != (B, T, Hv):
         raise ValueError("v [B,T,Hv,V], g [B,T,Hv,K] and beta [B,T,Hv] must match q [B,T,Hq,K]")
     if cu_seqlens is not None:
-        if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda or cu_seqlens.dim() != 1:
+        if cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1:
             raise ValueError("cu_seqlens must be a 1-D int32 CUDA tensor")
         if B != 1:
             raise ValueError("packed varlen inputs need B == 1")
@@ -49,6 +58,9 @@ def _check_inputs(q, k, v, g, beta, cu_seqlens, initial_state):
         if initial_state.dtype != torch.float32 or tuple(initial_state.shape) != (N, Hv, K, V):
             raise ValueError(f"initial_state must be float32 [{N}, {Hv}, {K}, {V}]")
     return B, T, Hq, Hv, K, V, N
+
+
+_PATHS = {"auto": _lib.KDA_PATH_AUTO, "fused": _lib.KDA_PATH_FUSED, "two_pass": _lib.KDA_PATH_TWO_PASS}
 
 
 def make_args(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=None):
@@ -72,7 +84,7 @@ def _contig(*ts):
 
 def chunk_kda_fwd(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=None,
                   output_final_state=True, return_intermediates=False, return_G=False, return_QG=False,
-                  tf32=False):
+                  tf32=False, path="auto", chunk_table=None):
     """Chunked KDA forward.  Returns (o, final_state, intermediates).
 
     ``intermediates`` is None unless ``return_intermediates`` (then a dict with
@@ -81,11 +93,24 @@ def chunk_kda_fwd(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=N
     query QG = q * e^G [B,T,Hv,K] bf16).  ``tf32`` selects the single-pass
     TF32 intra-chunk products (faster; Akk_inv near 5e-5 instead of 1e-6
     relative L2).  ``final_state`` is None unless
-    ``output_final_state``.
+    ``output_final_state``.  ``path`` picks the kernels: "auto", "fused" (one
+    kernel, each (sequence, head) chain on one SM) or "two_pass" (intra-chunk
+    kernel, then the state/output kernel).  ``chunk_table`` = (indices,
+    offsets) from ``prepare_chunk_indices`` reuses a varlen chunk table instead
+    of building it again on the device.
     """
+    if path not in _PATHS:
+        raise ValueError(f"path must be one of {sorted(_PATHS)}")
     q, k, v, g, beta, cu_seqlens, initial_state = _contig(q, k, v, g, beta, cu_seqlens, initial_state)
     a, (B, T, Hq, Hv, K, V, N) = make_args(q, k, v, g, beta, scale, initial_state, cu_seqlens)
+    a.path = _PATHS[path]
     dev = q.device
+    if chunk_table is not None:
+        idx, off = (t.contiguous() for t in chunk_table)
+        for name, t in (("chunk indices", idx), ("chunk offsets", off)):
+            if t.dtype != torch.int32 or not t.is_cuda or t.device != dev:
+                raise ValueError(f"{name} must be int32 CUDA tensors on {dev}")
+        a.chunk_indices, a.chunk_offsets = idx.data_ptr(), off.data_ptr()
     o = torch.empty(B, T, Hv, V, dtype=torch.bfloat16, device=dev)
     final = torch.empty(N, Hv, K, V, dtype=torch.float32, device=dev) if output_final_state else None
     inter = {} if (return_intermediates or return_G or return_QG) else None
@@ -106,7 +131,8 @@ def chunk_kda_fwd(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=N
         a.QG = _ptr(inter.get("QG"))
     ws_bytes = _lib.kda_workspace_size(a)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
-    rc = _lib.kda_chunk_fwd(a, ws.data_ptr(), ws_bytes, torch.cuda.current_stream(dev).cuda_stream)
+    with torch.cuda.device(dev):
+        rc = _lib.kda_chunk_fwd(a, ws.data_ptr(), ws_bytes, torch.cuda.current_stream(dev).cuda_stream)
     if rc != _lib.KDA_OK:
         raise KdaError(rc, "kda_chunk_fwd")
     return o, final, inter
@@ -134,7 +160,8 @@ def chunk_kda_fwd_intra(q, k, v, g, beta, scale=None, cu_seqlens=None, return_G=
     a.intra_tf32 = 1 if tf32 else 0
     ws_bytes = _lib.kda_workspace_size(a)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
-    rc = _lib.kda_fwd_intra(a, ws.data_ptr(), ws_bytes, torch.cuda.current_stream(dev).cuda_stream)
+    with torch.cuda.device(dev):
+        rc = _lib.kda_fwd_intra(a, ws.data_ptr(), ws_bytes, torch.cuda.current_stream(dev).cuda_stream)
     if rc != _lib.KDA_OK:
         raise KdaError(rc, "kda_fwd_intra")
     return out
@@ -166,8 +193,10 @@ def prepare_chunk_indices_device(cu_seqlens, T, chunk_size=_CHUNK):
     off = torch.empty(N + 1, dtype=torch.int32, device=dev)
     nc = torch.zeros(1, dtype=torch.int32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    rc = _lib.kda_prepare_chunk_indices(cu.data_ptr(), N, int(T), chunk_size, idx.data_ptr(), off.data_ptr(),
-                                        nc.data_ptr(), status.data_ptr(), torch.cuda.current_stream(dev).cuda_stream)
+    with torch.cuda.device(dev):
+        rc = _lib.kda_prepare_chunk_indices(cu.data_ptr(), N, int(T), chunk_size, idx.data_ptr(), off.data_ptr(),
+                                            nc.data_ptr(), status.data_ptr(),
+                                            torch.cuda.current_stream(dev).cuda_stream)
     if rc != _lib.KDA_OK:
         raise KdaError(rc, "kda_prepare_chunk_indices")
     return idx, off, nc, status
@@ -190,4 +219,6 @@ def prepare_chunk_indices(cu_seqlens, chunk_size=_CHUNK):
 
 def device_status(workspace: torch.Tensor) -> int:
     """Status word of a workspace after the work queued on the current stream."""
-    return _lib.kda_get_device_status(workspace.data_ptr(), torch.cuda.current_stream(workspace.device).cuda_stream)
+    with torch.cuda.device(workspace.device):
+        return _lib.kda_get_device_status(workspace.data_ptr(),
+                                          torch.cuda.current_stream(workspace.device).cuda_stream)

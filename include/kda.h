@@ -41,7 +41,12 @@
  *     The library allocates no device memory, keeps no state between calls,
  *     and performs no host<->device synchronisation; all work is enqueued on
  *     `stream` in order.  Calls on different streams with different
- *     workspaces are independent.
+ *     workspaces are independent.  The one exception is
+ *     kda_chunk_fwd_static_scratch (below): its workspace is a fixed array in
+ *     the library's device image, shared by every call, and the library keeps
+ *     that array's address per device.  Per-device facts (compute capability,
+ *     SM count, the kernels' shared memory attribute) are queried once and
+ *     cached for the life of the process.
  *   - Errors: host-side argument checks return a negative kda_status before
  *     anything is enqueued.  Errors found on the device (bad cu_seqlens, a
  *     bounded wait that ran out) are written to the status word at the start
@@ -79,8 +84,25 @@ enum kda_status {
   KDA_ERR_WORKSPACE = -6,    /* workspace smaller than kda_workspace_size() */
   KDA_ERR_BAD_SEQLENS = -16, /* (device) cu_seqlens not 0..T and non-decreasing */
   KDA_ERR_TIMEOUT = -17,     /* (device) a bounded wait inside a kernel ran out */
-  KDA_ERR_GATE_RANGE = -18   /* (device) a chunk's cumulative log-gate fell below -KDA_MAX_CHUNK_LOG_DECAY */
+  KDA_ERR_GATE_RANGE = -18,  /* (device) a chunk's cumulative log-gate fell below -KDA_MAX_CHUNK_LOG_DECAY */
+  KDA_ERR_BAD_CHUNK_TABLE = -19 /* (device) a caller-supplied chunk table does not match cu_seqlens */
 };
+
+/* Which kernels kda_chunk_fwd runs (KdaArgs.path).
+ *   KDA_PATH_AUTO      the fused forward, or the two-pass forward when the TF32
+ *                      option is set (only the two-pass kernels implement it).
+ *   KDA_PATH_FUSED     one kernel, one CTA per (sequence, value head) chain:
+ *                      the intra-chunk steps of chunk c+1 run next to the state
+ *                      and output steps of chunk c on the same SM, so the
+ *                      state pass's operands never reach HBM.  Chains are
+ *                      sequential over chunks; the path suits N * Hv of at
+ *                      least the SM count and long sequences.
+ *   KDA_PATH_TWO_PASS  a persistent intra-chunk kernel over all (chunk, head)
+ *                      items, then a state/output kernel over the chains; the
+ *                      state pass's operands go through the workspace.
+ * Both paths compute the same quantities with the same bf16/fp32 rounding
+ * points; their results agree within the accuracy bars, not bit for bit. */
+enum kda_path { KDA_PATH_AUTO = 0, KDA_PATH_FUSED = 1, KDA_PATH_TWO_PASS = 2 };
 
 enum kda_dtype { KDA_DTYPE_BF16 = 0, KDA_DTYPE_FP32 = 1 };
 
@@ -108,9 +130,10 @@ typedef struct KdaArgs {
   void* W;                     /* optional for kda_chunk_fwd, required for kda_fwd_intra */
   void* U;                     /* optional for kda_chunk_fwd, required for kda_fwd_intra */
   float* G;                    /* optional (both entry points) */
-  /* optional instrumentation: host array of 3 cudaEvent_t, recorded on
-   * `stream` before the first kernel, after the intra-chunk kernel and after
-   * the state/output kernel (kda_chunk_fwd); NULL = no events. */
+  /* optional instrumentation: host array of 3 cudaEvent_t recorded on
+   * `stream` (kda_chunk_fwd).  Two-pass path: before the intra-chunk kernel,
+   * after it, and after the state/output kernel.  Fused path: before and after
+   * the fused kernel, the third right after the second.  NULL = no events. */
   void* const* profile_events;
   /* optional output (both entry points; NULL = not written): the gated query
    * QG = q * e^G, bf16 [B, T, Hv, K], row t of value head hv from q of its
@@ -125,6 +148,20 @@ typedef struct KdaArgs {
    * points, cuLA PR #131, Numerical behavior).  o, the final state, W and U
    * stay within the same bars either way. */
   int32_t intra_tf32;
+  /* enum kda_path (kda_chunk_fwd; kda_fwd_intra ignores it).  Fused with the
+   * TF32 option is KDA_ERR_UNSUPPORTED. */
+  int32_t path;
+  /* Optional varlen chunk table built earlier by kda_prepare_chunk_indices (or
+   * by the caller, in its format), reused instead of being rebuilt on every call
+   * (the pages cache it for the same reason, cuLA PR #135 review of
+   * cula/ops/kda/index.py).  Device int32: chunk_indices [num_chunks, 2] pairs
+   * (sequence, chunk within sequence) in sequence order, chunk_offsets [N + 1]
+   * with chunk_offsets[N] = num_chunks.  Both NULL: built on the device into the
+   * workspace.  Both set: checked on the device against cu_seqlens before any
+   * kernel reads them; a mismatch sets KDA_ERR_BAD_CHUNK_TABLE and no output is
+   * written.  Only one of the two set is KDA_ERR_INVALID. */
+  const int32_t* chunk_indices;
+  const int32_t* chunk_offsets;
 } KdaArgs;
 
 typedef KdaArgs KdaFwdArgs;
@@ -192,12 +229,18 @@ int kda_check_bounded_wait(int32_t* device_status, kda_stream_t stream);
  *     library's device image, held on every GPU that loads the library until
  *     the process exits.  Nothing is allocated per call.
  *   - Problems whose kda_workspace_size(args) exceeds KDA_STATIC_SCRATCH_BYTES
- *     are rejected with KDA_ERR_WORKSPACE before any work is enqueued (at
- *     K = V = 128 that is about 57,000 token-heads with W and U NULL, about
- *     103,000 with W and U supplied).
+ *     are rejected with KDA_ERR_WORKSPACE before any work is enqueued.  The
+ *     fused path needs only a status header and, in varlen mode, the chunk
+ *     metadata (a few bytes per sequence and chunk), so any problem the other
+ *     entry points accept fits; the two-pass path (KdaArgs.path, or the TF32
+ *     option) keeps its state-pass operands there, which at K = V = 128 limits
+ *     it to about 57,000 token-heads with W and U NULL, about 103,000 with W
+ *     and U supplied.
  *   - The first call on a device looks up the array's device address (once
  *     per device, on the current device); make that first call before any
- *     stream capture.
+ *     stream capture.  The address is cached per process and device and does
+ *     not survive a cudaDeviceReset: after a reset, do not call this entry
+ *     point on that device again in the same process.
  *   - All calls share the one array, which keeps the last call's contents:
  *     calls whose GPU work overlaps (other streams, other host threads) race
  *     on it and must be serialised by the caller.  Each call resets the status

@@ -51,7 +51,7 @@ def test_struct_layout_matches_header(tmp_path):
 
 
 def test_status_strings(lib):
-    for code in (0, -1, -2, -3, -4, -5, -6, -16, -17, -18):
+    for code in (0, -1, -2, -3, -4, -5, -6, -16, -17, -18, -19):
         s = _lib.status_string(code)
         assert s and s != "unknown status"
     assert _lib.status_string(12345) == "unknown status"
@@ -100,19 +100,52 @@ def test_workspace_checks(lib):
     assert _lib.kda_workspace_size(_args(K=96)) == 0
 
 
-def test_workspace_size_accounts_for_missing_w_u(lib):
-    with_wu = _args(W=1 << 20, U=1 << 20)
-    without = _args()
-    # the state pass needs W and U: without caller buffers they live in the workspace
+def test_two_pass_workspace_accounts_for_missing_w_u(lib):
+    two = dict(path=_lib.KDA_PATH_TWO_PASS)
+    with_wu = _args(W=1 << 20, U=1 << 20, **two)
+    without = _args(**two)
+    # the two-pass state kernel reads W and U: without caller buffers they live in the workspace
     assert _lib.kda_workspace_size(without) - _lib.kda_workspace_size(with_wu) >= 2 * 128 * 2 * 64 * 2
+
+
+def test_fused_workspace_is_the_header_and_the_sequence_order(lib):
+    # the fused path keeps every state-pass operand on chip: the workspace holds
+    # the 256-byte status header, plus the longest-first sequence order (one
+    # int32 per sequence, rounded up to 256 bytes) in varlen mode
+    assert _lib.kda_workspace_size(_args()) == 256
+    assert _lib.kda_workspace_size(_args(path=_lib.KDA_PATH_FUSED, T=1 << 20, Hv=64, Hq=64)) == 256
+    # varlen: the fused forward needs 256 + 512 bytes; kda_workspace_size also
+    # covers kda_fwd_intra on the same arguments, whose chunk table takes
+    # (T/64 + N) pairs (1024 bytes) and N + 1 offsets (512)
+    varlen = _args(cu_seqlens=1 << 20, N=100)
+    assert _lib.kda_workspace_size(varlen) == 256 + 1024 + 512
+    assert _lib.kda_chunk_fwd(varlen, 1 << 24, 256 + 512 - 1, 0) == _lib.KDA_ERR_WORKSPACE
+    intra = _args(cu_seqlens=1 << 20, N=100, Aqk=1 << 20, Akk_inv=1 << 20, W=1 << 20, U=1 << 20)
+    assert _lib.kda_fwd_intra(intra, 1 << 24, 256 + 1024 + 512 - 1, 0) == _lib.KDA_ERR_WORKSPACE
 
 
 def test_workspace_size_ignores_optional_exports_and_precision(lib):
     # QG and the TF32 option change what the intra kernel writes and how it
-    # forms Aqk / Akk, not the workspace the call needs
-    base = _lib.kda_workspace_size(_args())
-    assert _lib.kda_workspace_size(_args(QG=1 << 20)) == base
+    # forms Aqk / Akk, not the two-pass workspace; with the automatic path the
+    # TF32 option selects the two-pass kernels, which need more
+    two = dict(path=_lib.KDA_PATH_TWO_PASS)
+    base = _lib.kda_workspace_size(_args(**two))
+    assert _lib.kda_workspace_size(_args(QG=1 << 20, **two)) == base
+    assert _lib.kda_workspace_size(_args(intra_tf32=1, **two)) == base
     assert _lib.kda_workspace_size(_args(intra_tf32=1)) == base
+    assert _lib.kda_workspace_size(_args(QG=1 << 20)) == _lib.kda_workspace_size(_args())
+
+
+@pytest.mark.parametrize("kw, code", [
+    (dict(path=7), _lib.KDA_ERR_INVALID),
+    (dict(path=_lib.KDA_PATH_FUSED, intra_tf32=1), _lib.KDA_ERR_UNSUPPORTED),
+    (dict(cu_seqlens=1 << 20, N=2, chunk_indices=1 << 20), _lib.KDA_ERR_INVALID),     # table without offsets
+    (dict(cu_seqlens=1 << 20, N=2, chunk_offsets=1 << 20), _lib.KDA_ERR_INVALID),     # offsets without table
+    (dict(cu_seqlens=1 << 20, N=2, chunk_indices=(1 << 20) + 2, chunk_offsets=1 << 20), _lib.KDA_ERR_MISALIGNED),
+])
+def test_path_and_chunk_table_arguments(lib, kw, code):
+    a = _args(**kw)
+    assert _lib.kda_chunk_fwd(a, 1 << 24, 1 << 30, 0) == code
 
 
 def test_intra_requires_its_outputs(lib):

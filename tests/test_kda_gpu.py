@@ -1,5 +1,9 @@
 """GPU parity of the CUDA path against the FP64 oracle, through the C ABI.
 
+Both forward paths are covered: the fused kernel (the default) and the
+two-pass kernels (intra-chunk, then state/output); PATHS parametrises the
+parity tests over them.
+
 Tolerances (floating point): o and final_state max |err| <= 2e-2 and relative
 L2 <= 5e-3 (bf16 I/O); Akk_inv and Aqk relative L2 <= 1e-4 (FP32 outputs of an
 ~FP32-accurate hi/lo-split product and an FP32 inverse); W, U elementwise
@@ -31,6 +35,9 @@ TOL_AQK_TF32 = dict(rel=1e-3)
 # QG = q e^G is rounded once from an FP32 product to bf16 (8 significant
 # bits): |err| <= 2^-8 |ref| plus the FP32 exp error
 TOL_QG = dict(atol=1e-6, rtol=2.0 ** -8 + 1e-5, rel=3e-3)
+
+
+PATHS = ["fused", "two_pass"]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -71,10 +78,11 @@ def _cuda(inp):
     return {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
 
 
-def _ours(inp, inter=True, G=False, QG=False, tf32=False):
+def _ours(inp, inter=True, G=False, QG=False, tf32=False, path="auto", chunk_table=None):
     return ops.chunk_kda_fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["scale"],
                              inp["initial_state"], inp["cu_seqlens"], output_final_state=True,
-                             return_intermediates=inter, return_G=G, return_QG=QG, tf32=tf32)
+                             return_intermediates=inter, return_G=G, return_QG=QG, tf32=tf32, path=path,
+                             chunk_table=chunk_table)
 
 
 def _check(name, got, want, max_abs=None, rel=None, atol=None, rtol=None):
@@ -123,11 +131,12 @@ SMALL_CASES = {
 }
 
 
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("case", sorted(SMALL_CASES))
-def test_small_cases_match_oracle(case):
+def test_small_cases_match_oracle(case, path):
     inp = make_inputs(WORKLOADS["tiny"], seed=100 + len(case), **SMALL_CASES[case])
     want = _oracle(inp)
-    out = _ours(_cuda(inp), inter=True, G=True, QG=True)
+    out = _ours(_cuda(inp), inter=True, G=True, QG=True, path=path)
     _compare(inp, out, want, inter=True)
 
 
@@ -149,26 +158,30 @@ def test_tf32_option_matches_oracle(case):
     _check("QG", _np(im["QG"]), want["QG"], **TOL_QG)
 
 
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("case", ["gva_init", "varlen"])
-def test_outputs_without_intermediates(case):
-    # W and U then live only in the workspace; o and the final state must
-    # match the oracle and, bit for bit, the call that exports them.
+def test_outputs_without_intermediates(case, path):
+    # Without exports (W and U then stay in the workspace on the two-pass
+    # path, on chip on the fused one) o and the final state must match the
+    # oracle and, bit for bit, the call that exports them.
     inp = make_inputs(WORKLOADS["tiny"], seed=200 + len(case), **SMALL_CASES[case])
     want = _oracle(inp)
     dev = _cuda(inp)
-    o, final, im = _ours(dev, inter=False)
+    o, final, im = _ours(dev, inter=False, path=path)
     assert im is None
     _check("o", _np(o), want["o"], **TOL_STATE)
     _check("final_state", _np(final), want["final_state"], **TOL_STATE)
-    o2, final2, _ = _ours(dev, inter=True)
+    o2, final2, _ = _ours(dev, inter=True, path=path)
     assert torch.equal(o, o2) and torch.equal(final, final2)
 
 
 def test_intra_primitive_matches_oracle_and_full_path():
+    # the standalone primitive runs the two-pass path's intra kernel: its
+    # outputs equal that path's exports bit for bit
     inp = _cuda(make_inputs(WORKLOADS["tiny"], seed=7, **SMALL_CASES["varlen"]))
     intra = ops.chunk_kda_fwd_intra(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["scale"],
                                     inp["cu_seqlens"], return_G=True, return_QG=True)
-    _, _, im = _ours(inp, inter=True, G=True, QG=True)
+    _, _, im = _ours(inp, inter=True, G=True, QG=True, path="two_pass")
     for key in ("Aqk", "Akk_inv", "W", "U", "G", "QG"):
         assert torch.equal(intra[key], im[key]), key
     want = _oracle({k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()})
@@ -176,9 +189,10 @@ def test_intra_primitive_matches_oracle_and_full_path():
     _check("W", _np(intra["W"]), want["W"], **TOL_WU)
 
 
-def test_inverse_identity_on_gpu_output():
+@pytest.mark.parametrize("path", PATHS)
+def test_inverse_identity_on_gpu_output(path):
     inp = make_inputs(WORKLOADS["mha_1k"], T=256, B=1, Hq=4, Hv=4)
-    _, _, im = _ours(_cuda(inp), inter=True, G=True)
+    _, _, im = _ours(_cuda(inp), inter=True, G=True, path=path)
     want = _oracle(inp)
     # (I + Akk) Akk_inv = I with the oracle's Akk and the GPU's inverse
     A = want["Akk"][0, :64, 0, :64]
@@ -187,6 +201,10 @@ def test_inverse_identity_on_gpu_output():
 
 
 # --------------------------------------------------------------- workloads
+_ORACLE_CACHE = {}
+
+
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("name, heads", [
     ("tiny", None),
     ("mha_1k", [0, 17, 63]),
@@ -194,11 +212,13 @@ def test_inverse_identity_on_gpu_output():
     ("gva_4k", [0, 5, 63]),
     ("varlen_16k", [0, 33]),
 ])
-def test_workload_matches_oracle(name, heads):
+def test_workload_matches_oracle(name, heads, path):
     w = WORKLOADS[name]
     inp = make_inputs(w)
-    want = _oracle(inp, heads=heads)
-    out = _ours(_cuda(inp), inter=True)
+    if name not in _ORACLE_CACHE:
+        _ORACLE_CACHE[name] = _oracle(inp, heads=heads)
+    want = _ORACLE_CACHE[name]
+    out = _ours(_cuda(inp), inter=True, path=path)
     _compare(inp, out, want, heads=heads, inter=True)
 
 
@@ -225,10 +245,12 @@ def test_chunk_indices_reject_bad_metadata():
             ops.prepare_chunk_indices(torch.tensor([0, 4], dtype=torch.int32, device="cuda"), bad)
 
 
-def test_bad_cu_seqlens_sets_device_status():
+@pytest.mark.parametrize("path", PATHS)
+def test_bad_cu_seqlens_sets_device_status(path):
     inp = _cuda(make_inputs(WORKLOADS["tiny"], lengths=(100, 156)))
     a, _ = ops.make_args(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["scale"], None,
                          inp["cu_seqlens"])
+    a.path = ops._PATHS[path]
     o = torch.zeros(1, 256, 2, 64, dtype=torch.bfloat16, device="cuda")
     a.o = o.data_ptr()
     bad = torch.tensor([0, 150, 100], dtype=torch.int32, device="cuda")  # decreasing
@@ -244,7 +266,48 @@ def test_bad_cu_seqlens_sets_device_status():
     assert ops.device_status(ws) == _lib.KDA_OK
 
 
-def test_strong_gates_within_range_match_oracle():
+@pytest.mark.parametrize("path", PATHS)
+def test_caller_chunk_table_gives_the_same_results(path):
+    # a chunk table built once by kda_prepare_chunk_indices and passed back in
+    # (checked on the device, then used by the two-pass kernels) gives the
+    # results of the call that builds its own, bit for bit
+    inp = _cuda(make_inputs(WORKLOADS["tiny"], seed=71, **SMALL_CASES["varlen"]))
+    table = ops.prepare_chunk_indices(inp["cu_seqlens"], 64)
+    ref_out = _ours(inp, inter=True, path=path)
+    out = _ours(inp, inter=True, path=path, chunk_table=table)
+    assert torch.equal(ref_out[0], out[0]) and torch.equal(ref_out[1], out[1])
+    for key in ref_out[2]:
+        assert torch.equal(ref_out[2][key], out[2][key]), key
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_bad_caller_chunk_table_sets_device_status(path):
+    inp = _cuda(make_inputs(WORKLOADS["tiny"], seed=72, lengths=(100, 30, 156)))
+    idx, off = ops.prepare_chunk_indices(inp["cu_seqlens"], 64)
+    stream = torch.cuda.current_stream().cuda_stream
+    cases = []
+    swapped = idx.clone()
+    swapped[[0, 1]] = swapped[[1, 0]]            # two pairs out of order
+    cases.append((swapped, off))
+    shifted = off.clone()
+    shifted[1:] += 1                             # offsets that skip a row
+    cases.append((idx, shifted))
+    for t_idx, t_off in cases:
+        a, (B, T, Hq, Hv, K, V, N) = ops.make_args(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+                                                   inp["scale"], None, inp["cu_seqlens"])
+        a.path = ops._PATHS[path]
+        a.chunk_indices, a.chunk_offsets = t_idx.data_ptr(), t_off.data_ptr()
+        o = torch.zeros(B, T, Hv, V, dtype=torch.bfloat16, device="cuda")
+        a.o = o.data_ptr()
+        n = _lib.kda_workspace_size(a)
+        ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+        assert _lib.kda_chunk_fwd(a, ws.data_ptr(), n, stream) == _lib.KDA_OK
+        assert ops.device_status(ws) == _lib.KDA_ERR_BAD_CHUNK_TABLE
+        assert torch.count_nonzero(o) == 0
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_strong_gates_within_range_match_oracle(path):
     # A per-step log-gate of -0.9 on every other channel: each full chunk then
     # decays by 57.6 on those channels, just inside KDA_MAX_CHUNK_LOG_DECAY, so
     # the operands q e^G and k e^-G span about 25 decades.
@@ -253,15 +316,17 @@ def test_strong_gates_within_range_match_oracle():
     g[..., ::2] = -0.9
     inp["g"] = g
     want = _oracle(inp)
-    out = _ours(_cuda(inp), inter=True)
+    out = _ours(_cuda(inp), inter=True, path=path)
     _compare(inp, out, want, inter=True)
 
 
-def test_gates_past_the_range_set_device_status():
+@pytest.mark.parametrize("path", PATHS)
+def test_gates_past_the_range_set_device_status(path):
     inp = _cuda(make_inputs(WORKLOADS["tiny"], seed=44, T=128))
     inp["g"][:, 64:, 1, 5] = -1.0  # the second chunk decays by 64 on one channel of head 1
     a, (B, T, Hq, Hv, K, V, N) = ops.make_args(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
                                                inp["scale"], None, None)
+    a.path = ops._PATHS[path]
     o = torch.zeros(B, T, Hv, V, dtype=torch.bfloat16, device="cuda")
     a.o = o.data_ptr()
     n = _lib.kda_workspace_size(a)
@@ -275,13 +340,14 @@ def test_gates_past_the_range_set_device_status():
     assert ops.device_status(ws) == _lib.KDA_OK
 
 
-def test_zero_beta_is_pure_gated_decay():
+@pytest.mark.parametrize("path", PATHS)
+def test_zero_beta_is_pure_gated_decay(path):
     # beta = 0: no delta updates.  Akk = 0, so Akk_inv is the identity and W, U
     # vanish exactly; the state only decays, S_T = Diag(e^{sum_t g_t}) S0, and
     # o_t = scale S0^T (q_t * e^{sum_{j<=t} g_j}) in closed form.
     inp = make_inputs(WORKLOADS["tiny"], seed=47, T=200, initial_state=True)
     inp["beta"] = torch.zeros_like(inp["beta"])
-    o, final, im = _ours(_cuda(inp), inter=True)
+    o, final, im = _ours(_cuda(inp), inter=True, path=path)
     q = inp["q"].double().numpy()[0]              # [T, H, K]
     g = inp["g"].double().numpy()[0]              # [T, H, K]
     S0 = inp["initial_state"].double().numpy()[0]  # [H, K, V]
@@ -310,16 +376,18 @@ def test_bounded_wait_gives_up_and_reports_timeout():
     _compare(inp, _ours(_cuda(inp), inter=True), _oracle(inp), inter=True)
 
 
-def test_empty_inputs():
+@pytest.mark.parametrize("path", PATHS)
+def test_empty_inputs(path):
     inp = _cuda(make_inputs(WORKLOADS["tiny"], T=0, initial_state=True))
-    o, final, _ = _ours(inp, inter=False)
+    o, final, _ = _ours(inp, inter=False, path=path)
     assert o.numel() == 0 and torch.equal(final, inp["initial_state"])
     inp = _cuda(make_inputs(WORKLOADS["tiny"], lengths=(0, 0), initial_state=True))
-    o, final, _ = _ours(inp, inter=False)
+    o, final, _ = _ours(inp, inter=False, path=path)
     assert torch.equal(final, inp["initial_state"])
 
 
-def test_nonfinite_values_stay_in_their_sequence():
+@pytest.mark.parametrize("path", PATHS)
+def test_nonfinite_values_stay_in_their_sequence(path):
     # Packed varlen: sequence 0 ends in a tail chunk (tokens 64-99, L = 36)
     # whose 64-row TMA boxes (v in the intra kernel, Kl in the state kernel)
     # also cover the first tokens of sequence 1.  NaN / Inf planted in v and k
@@ -332,7 +400,7 @@ def test_nonfinite_values_stay_in_their_sequence():
     bad["v"][0, 120, 0, :] = float("inf")
     bad["k"][0, 105, 0, 7] = float("nan")
     bad["k"][0, 126, 1, :] = float("inf")
-    o, final, _ = _ours(_cuda(bad), inter=True)
+    o, final, _ = _ours(_cuda(bad), inter=True, path=path)
     seq0 = make_inputs(WORKLOADS["tiny"], seed=61, lengths=(100, 50), Hq=2, Hv=2, K=128, V=128,
                        initial_state=True)
     for key in ("q", "k", "v", "g", "beta"):
@@ -345,32 +413,35 @@ def test_nonfinite_values_stay_in_their_sequence():
     _check("final_state", _np(final[:1]), want["final_state"], **TOL_STATE)
 
 
-def test_replay_is_bitwise_deterministic():
+@pytest.mark.parametrize("path", PATHS)
+def test_replay_is_bitwise_deterministic(path):
     inp = _cuda(make_inputs(WORKLOADS["varlen_16k"], varlen_total=4096, Hq=8, Hv=8))
-    first = _ours(inp, inter=True)
+    first = _ours(inp, inter=True, path=path)
     for _ in range(3):
-        again = _ours(inp, inter=True)
+        again = _ours(inp, inter=True, path=path)
         assert torch.equal(first[0], again[0]) and torch.equal(first[1], again[1])
         for key in first[2]:
             assert torch.equal(first[2][key], again[2][key]), key
 
 
-def test_two_streams_give_identical_results():
+@pytest.mark.parametrize("path", PATHS)
+def test_two_streams_give_identical_results(path):
     a = _cuda(make_inputs(WORKLOADS["mha_1k"], seed=11, B=1, Hq=16, Hv=16))
     b = _cuda(make_inputs(WORKLOADS["gva_4k"], seed=12, T=1024, Hq=4, Hv=16))
-    ref_a, ref_b = _ours(a), _ours(b)
+    ref_a, ref_b = _ours(a, path=path), _ours(b, path=path)
     s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
     torch.cuda.synchronize()
     with torch.cuda.stream(s1):
-        out_a = _ours(a)
+        out_a = _ours(a, path=path)
     with torch.cuda.stream(s2):
-        out_b = _ours(b)
+        out_b = _ours(b, path=path)
     torch.cuda.synchronize()
     assert torch.equal(ref_a[0], out_a[0]) and torch.equal(ref_a[1], out_a[1])
     assert torch.equal(ref_b[0], out_b[0]) and torch.equal(ref_b[1], out_b[1])
 
 
-def test_poisoned_workspace_does_not_leak():
+@pytest.mark.parametrize("path", PATHS)
+def test_poisoned_workspace_does_not_leak(path):
     # every workspace byte starts as a NaN pattern: results must equal a run on
     # a zeroed workspace, bit for bit (nothing reads workspace it did not write)
     inp = _cuda(make_inputs(WORKLOADS["tiny"], seed=5, **SMALL_CASES["varlen"]))
@@ -378,6 +449,7 @@ def test_poisoned_workspace_does_not_leak():
     for fill in (0x00, 0xFF):
         a, (B, T, Hq, Hv, K, V, N) = ops.make_args(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
                                                    inp["scale"], inp["initial_state"], inp["cu_seqlens"])
+        a.path = ops._PATHS[path]
         o = torch.full((B, T, Hv, V), float("nan"), dtype=torch.bfloat16, device="cuda")
         fin = torch.full((N, Hv, K, V), float("nan"), dtype=torch.float32, device="cuda")
         a.o, a.final_state = o.data_ptr(), fin.data_ptr()
@@ -390,16 +462,17 @@ def test_poisoned_workspace_does_not_leak():
     assert torch.isfinite(outs[0][0].float()).all() and torch.isfinite(outs[0][1]).all()
 
 
-def test_continuation_across_calls():
+@pytest.mark.parametrize("path", PATHS)
+def test_continuation_across_calls(path):
     inp = make_inputs(WORKLOADS["mha_1k"], seed=21, B=1, Hq=4, Hv=4, initial_state=True)
-    full = _ours(_cuda(inp), inter=False)
+    full = _ours(_cuda(inp), inter=False, path=path)
     T1 = 384 + 17
     seq = ("q", "k", "v", "g", "beta")
     first = {k: (v[:, :T1] if k in seq else v) for k, v in inp.items()}
     second = {k: (v[:, T1:] if k in seq else v) for k, v in inp.items()}
     first["T"], second["T"] = T1, inp["T"] - T1
-    r1 = _ours(_cuda(first), inter=False)
+    r1 = _ours(_cuda(first), inter=False, path=path)
     second["initial_state"] = r1[1].cpu()
-    r2 = _ours(_cuda(second), inter=False)
+    r2 = _ours(_cuda(second), inter=False, path=path)
     _check("o", _np(r2[0]), _np(full[0])[:, T1:], **TOL_STATE)
     _check("final_state", _np(r2[1]), _np(full[1]), **TOL_STATE)

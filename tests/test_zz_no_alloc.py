@@ -3,15 +3,20 @@
 Plug-ins that a host runtime hands only input and output buffers (the runtime
 owns the device memory pool), and latency-critical code that must not
 allocate, call this variant: it runs the same kernels as kda_chunk_fwd on a
-fixed scratch array inside the library instead of a caller workspace.  This
-test calls it through the C ABI, twice in a row, and checks every output
-against the ordinary entry point's within the parity tolerances of
-test_kda_gpu.py; it also checks that a problem too large for the fixed scratch
-is refused before any work is queued.  It lives in its own file so that pytest
-collects it last.
+fixed scratch array inside the library instead of a caller workspace.  These
+tests call it through the C ABI:
+
+* twice in a row on two problems, on both forward paths: every output equals
+  the ordinary entry point's bit for bit (same kernels on the same inputs;
+  a stale read of the shared array would show up as a difference);
+* a device-side error (a decreasing cu_seqlens) reaches its device_status
+  output, and the next valid call on the same shared array starts clean;
+* a problem too large for the fixed scratch is refused before any work is
+  queued.
+
+It lives in its own file so that pytest collects it last.
 """
 
-import numpy as np
 import pytest
 import torch
 
@@ -20,33 +25,27 @@ from chunked_gated_delta_03_gb300.workloads import WORKLOADS, make_inputs
 
 pytestmark = pytest.mark.gpu
 
-TOL = {"o": (2e-2, 5e-3), "final_state": (2e-2, 5e-3), "Aqk": (None, 1e-4), "Akk_inv": (None, 1e-4),
-       "W": (2e-2, 5e-3), "U": (2e-2, 5e-3)}
+KEYS = ("o", "final_state", "Aqk", "Akk_inv", "W", "U")
 
 
-def _close(name, got, want):
-    got = got.double().cpu().numpy()
-    want = want.double().cpu().numpy()
-    atol, rel = TOL[name]
-    assert np.all(np.isfinite(got)), name
-    err = np.abs(got - want)
-    if atol is not None:
-        assert np.all(err <= atol + 1e-2 * np.abs(want)), f"{name}: max err {err.max():.3e}"
-    denom = max(np.linalg.norm(want), 1e-30)
-    assert np.linalg.norm(got - want) / denom <= rel, name
-
-
-def _static_call(inp):
-    a, (B, T, Hq, Hv, K, V, N) = ops.make_args(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["scale"],
-                                               inp["initial_state"], inp["cu_seqlens"])
-    out = {
-        "o": torch.full((B, T, Hv, V), float("nan"), dtype=torch.bfloat16, device="cuda"),
-        "final_state": torch.full((N, Hv, K, V), float("nan"), dtype=torch.float32, device="cuda"),
-        "Aqk": torch.full((B, T, Hv, 64), float("nan"), dtype=torch.float32, device="cuda"),
-        "Akk_inv": torch.full((B, T, Hv, 64), float("nan"), dtype=torch.float32, device="cuda"),
-        "W": torch.full((B, T, Hv, K), float("nan"), dtype=torch.bfloat16, device="cuda"),
-        "U": torch.full((B, T, Hv, V), float("nan"), dtype=torch.bfloat16, device="cuda"),
+def _outputs(B, T, Hv, K, V, N):
+    nan = float("nan")
+    return {
+        "o": torch.full((B, T, Hv, V), nan, dtype=torch.bfloat16, device="cuda"),
+        "final_state": torch.full((N, Hv, K, V), nan, dtype=torch.float32, device="cuda"),
+        "Aqk": torch.full((B, T, Hv, 64), nan, dtype=torch.float32, device="cuda"),
+        "Akk_inv": torch.full((B, T, Hv, 64), nan, dtype=torch.float32, device="cuda"),
+        "W": torch.full((B, T, Hv, K), nan, dtype=torch.bfloat16, device="cuda"),
+        "U": torch.full((B, T, Hv, V), nan, dtype=torch.bfloat16, device="cuda"),
     }
+
+
+def _static_call(inp, path, cu=None):
+    cu = inp["cu_seqlens"] if cu is None else cu
+    a, (B, T, Hq, Hv, K, V, N) = ops.make_args(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["scale"],
+                                               inp["initial_state"], cu)
+    a.path = ops._PATHS[path]
+    out = _outputs(B, T, Hv, K, V, N)
     a.o, a.final_state = out["o"].data_ptr(), out["final_state"].data_ptr()
     a.Aqk, a.Akk_inv = out["Aqk"].data_ptr(), out["Akk_inv"].data_ptr()
     a.W, a.U = out["W"].data_ptr(), out["U"].data_ptr()
@@ -55,8 +54,7 @@ def _static_call(inp):
     rc = _lib.kda_chunk_fwd_static_scratch(a, status.data_ptr(), torch.cuda.current_stream().cuda_stream)
     assert rc == _lib.KDA_OK, _lib.status_string(rc)
     torch.cuda.synchronize()
-    assert int(status.item()) == _lib.KDA_OK
-    return out
+    return out, int(status.item())
 
 
 CASES = {
@@ -66,21 +64,49 @@ CASES = {
 }
 
 
-def test_static_scratch_matches_workspace_entry_point():
-    build.build()
-    _lib.load()
+def _inputs():
     inputs = {}
     for name, kw in CASES.items():
         host = make_inputs(WORKLOADS["tiny"], **kw)
         inputs[name] = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in host.items()}
+    return inputs
+
+
+@pytest.mark.parametrize("path", ["fused", "two_pass"])
+def test_static_scratch_matches_workspace_entry_point(path):
+    build.build()
+    _lib.load()
+    inputs = _inputs()
     for _ in range(2):  # two calls in a row on the shared scratch
         for name, inp in inputs.items():
             o, fin, im = ops.chunk_kda_fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["scale"],
-                                           inp["initial_state"], inp["cu_seqlens"], return_intermediates=True)
-            got = _static_call(inp)
+                                           inp["initial_state"], inp["cu_seqlens"], return_intermediates=True,
+                                           path=path)
+            got, status = _static_call(inp, path)
+            assert status == _lib.KDA_OK, _lib.status_string(status)
             want = {"o": o, "final_state": fin, **im}
-            for key in TOL:
-                _close(key, got[key], want[key])
+            for key in KEYS:
+                assert torch.equal(got[key], want[key]), f"{name} {key}"
+
+
+@pytest.mark.parametrize("path", ["fused", "two_pass"])
+def test_static_scratch_reports_device_errors_then_recovers(path):
+    build.build()
+    _lib.load()
+    inp = _inputs()["varlen_gva"]
+    bad = inp["cu_seqlens"].clone()
+    bad[3], bad[4] = bad[4], bad[3]  # no longer non-decreasing
+    got, status = _static_call(inp, path, cu=bad)
+    assert status == _lib.KDA_ERR_BAD_SEQLENS
+    assert torch.isnan(got["o"].float()).all()  # the kernels saw the status and wrote nothing
+    # the next valid call on the same shared array starts from a clean status
+    o, fin, im = ops.chunk_kda_fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["scale"],
+                                   inp["initial_state"], inp["cu_seqlens"], return_intermediates=True, path=path)
+    got, status = _static_call(inp, path)
+    assert status == _lib.KDA_OK
+    want = {"o": o, "final_state": fin, **im}
+    for key in KEYS:
+        assert torch.equal(got[key], want[key]), key
 
 
 def test_static_scratch_refuses_oversized_problems():
@@ -90,5 +116,6 @@ def test_static_scratch_refuses_oversized_problems():
     base = 1 << 20  # never dereferenced: the size check comes first
     a.q = a.k = a.v = a.g = a.beta = a.o = base
     a.B, a.T, a.Hq, a.Hv, a.K, a.V, a.chunk, a.scale = 2, 8192, 64, 64, 128, 128, 64, 0.088
+    a.path = _lib.KDA_PATH_TWO_PASS  # the two-pass path keeps its state-pass operands in the scratch
     assert _lib.kda_workspace_size(a) > _lib.KDA_STATIC_SCRATCH_BYTES
     assert _lib.kda_chunk_fwd_static_scratch(a, 0, 0) == _lib.KDA_ERR_WORKSPACE

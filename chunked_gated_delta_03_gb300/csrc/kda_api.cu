@@ -334,6 +334,7 @@ int fused_forward(const Shape& s, const KdaArgs* a, uint8_t* ws, const Layout& L
   f.U = a->U;
   f.G = a->G;
   f.QG = a->QG;
+  f.aqk_v8 = (reinterpret_cast<uintptr_t>(a->Aqk) & 31u) == 0;
   if (launch_fused(P, f, m, d.dev, st) != cudaSuccess) return KDA_ERR_LAUNCH;
   if (ev && (cudaEventRecord(ev[1], st) != cudaSuccess || cudaEventRecord(ev[2], st) != cudaSuccess))
     return KDA_ERR_LAUNCH;

@@ -15,15 +15,17 @@
 //   w8-w11   intra epilogue: Aqk rows (scale, causal mask) from D1 to the
 //            fp32 export and to a bf16 operand tile; Akk rows (beta, strict
 //            mask) to shared memory; the FP32 inverse X = (I + Akk)^-1 by
-//            16 x 16 blocks on all 128 threads; B2 = X diag(beta) as a bf16
-//            tile; the Akk_inv export; W^T from TMEM into the state pass's
-//            operand tile and the W / U exports.  w8 lane 0 issues MMA2
+//            16 x 16 blocks (diagonal blocks by forward substitution, the
+//            off-diagonal products as warp-level TF32 hi/lo MMAs), writing
+//            B2 = X diag(beta) as a bf16 tile as it goes; the Akk_inv export.  w8 lane 0 issues MMA2
 //            (W^T = Kg^T B2^T, U^T = v^T B2^T), the TMA copy of each chunk's v
 //            into its operand tile and the L2 prefetch of the next chunk's
 //            q, k, v, g; a tail chunk's v rows past its end are cleared.
 //   w12-w15  state (thread = value channel v): S^T lives in TMEM in fp32 and
-//            as a bf16 copy in shared memory (the A operand).  Per chunk, w12
-//            lane 0 issues P^T = S^T W^T and O^T = S^T Qg^T, the threads form
+//            as a bf16 copy in shared memory (the A operand).  Per chunk, the
+//            threads copy W^T from TMEM into the W operand tile (and export W
+//            and U, thread = channel), w12 lane 0
+//            issues P^T = S^T W^T and O^T = S^T Qg^T, the threads form
 //            Delta^T = U^T - P^T (rows past the chunk's end zero), w12 lane 0
 //            issues S^T += Delta^T Kd and O^T += Delta^T Aqk^T, and the
 //            threads scale the state by gamma:
@@ -96,15 +98,29 @@ enum {
   bLoFree = 3,   // intra epilogue done with the scratch in the lo area -> prep  (128)
   bHiFree = 4,   // [2] state done with hi buffer b (and its gamma) -> prep, Aqk (128)
   bVFull = 6,    // TMA: v chunk landed                                          (1 + bytes)
-  bD2Full = 7,   // MMA2 done -> intra epilogue, state                           (commit)
-  bD2Empty = 8,  // W^T / U^T read -> MMA2                                       (256)
-  bWFull = 9,    // W tile and Aqk_b written -> state MMA issue                  (128)
+  bD2Full = 7,   // MMA2 done (after Aqk_b was written) -> intra epilogue, state (commit)
+  bD2Empty = 8,  // state read W^T / U^T -> MMA2                                (128)
   bPDone = 10,   // P^T and O^T = S^T Qg^T done -> state                         (commit)
   bHODone = 11,  // S^T += Delta^T Kd and O^T += Delta^T Aqk^T done              (commit)
   bDrain = 12,   // [3] final drains of the three MMA issuers                    (commit)
 };
 
 __device__ __forceinline__ uint32_t par(int n) { return uint32_t(n) & 1u; }
+
+// Register budgets per warpgroup (setmaxnreg; the kernel launches with 128 a
+// thread, 65536 in all): the prep warpgroups take 160, the intra warpgroup
+// 104, the state warpgroup 88 -- 2 x 128 x 160 + 128 x 104 + 128 x 88 = 65536,
+// so the increase never waits for registers that are not there.
+constexpr uint32_t kRegsPrep = 160, kRegsIntra = 104, kRegsState = 88;
+static_assert(2 * 128 * kRegsPrep + 128 * kRegsIntra + 128 * kRegsState <= 65536, "register split");
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
 
 __device__ __forceinline__ float exp2f_fast(float x) {
   float y;
@@ -136,6 +152,115 @@ __device__ __forceinline__ float4 fma4(float a, float4 x, float4 acc) {
   acc.z = fmaf(a, x.z, acc.z);
   acc.w = fmaf(a, x.w, acc.w);
   return acc;
+}
+
+// fp32 x -> (hi, lo) TF32 bit patterns with x ~ hi + lo: hi rounded to nearest
+// TF32, lo the TF32 rounding of the remainder
+__device__ __forceinline__ void tf32_split(float x, uint32_t& hi, uint32_t& lo) {
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(hi) : "f"(x));
+  const float r = x - __uint_as_float(hi);
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(lo) : "f"(r));
+}
+
+// d0, d1 (16 x 8 each: the mma.m16n8k8 accumulator fragments of columns 0-7
+// and 8-15) = A (16 x [k0, k1)) B ([k0, k1) x 16) on the warp's tensor cores,
+// from fp32 tiles in shared memory (A row-major, stride lda; B row-major,
+// stride ldb), each product as three TF32 products (hi*hi + hi*lo + lo*hi:
+// close to fp32 accuracy).  The three partial products and the two column
+// halves accumulate separately, so the six chains of dependent MMAs overlap.
+// Fragments of the m16n8k8 TF32 shape: lane = 4 g + t holds A[g][t],
+// A[g+8][t], A[g][t+4], A[g+8][t+4], B[t][g], B[t+4][g], and D[g][2t],
+// D[g][2t+1], D[g+8][2t], D[g+8][2t+1].
+__device__ __forceinline__ void mma_3xtf32_x2(float (&d0)[4], float (&d1)[4], const float* A, int lda,
+                                              const float* B, int ldb, int k0, int k1) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  float acc[6][4];
+#pragma unroll
+  for (int i = 0; i < 6; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+#define KDA_MMA_TF32(c, a, b)                                                                                 \
+  asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "  \
+               "{%0,%1,%2,%3};"                                                                               \
+               : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])                                              \
+               : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]))
+#pragma unroll 1
+  for (int k = k0; k < k1; k += 8) {
+    uint32_t ah[4], al[4], bh[2][2], bl[2][2];
+    tf32_split(A[g * lda + k + t], ah[0], al[0]);
+    tf32_split(A[(g + 8) * lda + k + t], ah[1], al[1]);
+    tf32_split(A[g * lda + k + t + 4], ah[2], al[2]);
+    tf32_split(A[(g + 8) * lda + k + t + 4], ah[3], al[3]);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      tf32_split(B[(k + t) * ldb + 8 * h + g], bh[h][0], bl[h][0]);
+      tf32_split(B[(k + t + 4) * ldb + 8 * h + g], bh[h][1], bl[h][1]);
+    }
+    KDA_MMA_TF32(acc[0], ah, bh[0]);
+    KDA_MMA_TF32(acc[1], ah, bh[1]);
+    KDA_MMA_TF32(acc[2], ah, bl[0]);
+    KDA_MMA_TF32(acc[3], ah, bl[1]);
+    KDA_MMA_TF32(acc[4], al, bh[0]);
+    KDA_MMA_TF32(acc[5], al, bh[1]);
+  }
+#undef KDA_MMA_TF32
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    d0[e] = acc[0][e] + (acc[2][e] + acc[4][e]);
+    d1[e] = acc[1][e] + (acc[3][e] + acc[5][e]);
+  }
+}
+
+// d (16 x 8) = A (16 x [k0, k1)) B ([k0, k1) x 8), as mma_3xtf32_x2 with one
+// column half (three independent accumulation chains).
+__device__ __forceinline__ void mma_3xtf32_x1(float (&d)[4], const float* A, int lda, const float* B, int ldb,
+                                              int k0, int k1) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  float acc[3][4];
+#pragma unroll
+  for (int i = 0; i < 3; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+#define KDA_MMA_TF32(c, a, b)                                                                                 \
+  asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "  \
+               "{%0,%1,%2,%3};"                                                                               \
+               : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])                                              \
+               : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]))
+#pragma unroll
+  for (int k = k0; k < k1; k += 8) {
+    uint32_t ah[4], al[4], bh[2], bl[2];
+    tf32_split(A[g * lda + k + t], ah[0], al[0]);
+    tf32_split(A[(g + 8) * lda + k + t], ah[1], al[1]);
+    tf32_split(A[g * lda + k + t + 4], ah[2], al[2]);
+    tf32_split(A[(g + 8) * lda + k + t + 4], ah[3], al[3]);
+    tf32_split(B[(k + t) * ldb + g], bh[0], bl[0]);
+    tf32_split(B[(k + t + 4) * ldb + g], bh[1], bl[1]);
+    KDA_MMA_TF32(acc[0], ah, bh);
+    KDA_MMA_TF32(acc[1], ah, bl);
+    KDA_MMA_TF32(acc[2], al, bh);
+  }
+#undef KDA_MMA_TF32
+#pragma unroll
+  for (int e = 0; e < 4; ++e) d[e] = acc[0][e] + (acc[1][e] + acc[2][e]);
+}
+
+// The fragment d (16 x 8 at rows r0.., columns c0..) scaled by s into X (fp32,
+// row-major, stride kLd) and, times beta of each column, into the bf16 B2 tile.
+__device__ __forceinline__ void store_x_b2(float* X, uint8_t* b2, const float* sB, int r0, int c0,
+                                           const float (&d)[4], float s) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  const int c = c0 + 2 * t;
+  const float b0 = sB[c], b1 = sB[c + 1];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int r = r0 + g + 8 * h;
+    const float x0 = s * d[2 * h], x1 = s * d[2 * h + 1];
+    *reinterpret_cast<float2*>(X + r * kLd + c) = make_float2(x0, x1);
+    *reinterpret_cast<uint32_t*>(b2 + sw128_offset(uint32_t(r), uint32_t(c), 64)) = pack_bf16x2(x0 * b0, x1 * b1);
+  }
+}
+
+// Stores s * d (the accumulator fragment) at C (row-major, stride ldc).
+__device__ __forceinline__ void store_frag(float* C, int ldc, const float (&d)[4], float s) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  *reinterpret_cast<float2*>(C + g * ldc + 2 * t) = make_float2(s * d[0], s * d[1]);
+  *reinterpret_cast<float2*>(C + (g + 8) * ldc + 2 * t) = make_float2(s * d[2], s * d[3]);
 }
 
 template <int K, int V, bool kQG>
@@ -183,8 +308,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     mbar_init(&bar[bHiFree + 1], 128);
     mbar_init(&bar[bVFull], 1);
     mbar_init(&bar[bD2Full], 1);
-    mbar_init(&bar[bD2Empty], 256);
-    mbar_init(&bar[bWFull], 128);
+    mbar_init(&bar[bD2Empty], 128);
     mbar_init(&bar[bPDone], 1);
     mbar_init(&bar[bHODone], 1);
     for (int i = 0; i < 3; ++i) mbar_init(&bar[bDrain + i], 1);
@@ -202,6 +326,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
 
   if (warp < kWarpIntra0) {
     // ================================================================ prep
+    regs_inc<kRegsPrep>();
     const int ptid = tid;
     const bool mma_leader = ptid == 0;  // issues MMA1
     const int p = ptid & 63, quarter = ptid >> 6, c0 = 2 * p;
@@ -218,6 +343,14 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     uint8_t* lo = sm + Lay::LO;
     for (int c = 0; c < nch; ++c) {
       const int t0 = bos + c * kChunk, L = min(kChunk, len - c * kChunk);
+      // ---- L2 prefetch of the next chunk's q, k, v and g (a box of 64 token
+      // rows of one head each, one per thread of lanes 0 of warps 0-3), a whole
+      // chunk period ahead of its loads
+      if (lane == 0 && warp < 4 && c + 1 < nch) {
+        const int tn = t0 + kChunk;
+        const CUtensorMap* m = warp == 0 ? &maps.q : warp == 1 ? &maps.k : warp == 2 ? &maps.v : &maps.g;
+        tma_prefetch_l2_3d(m, 0, warp < 2 ? hq : hv, tn);
+      }
       // ---- loads (all in flight together)
       float2 g2[kRows];
       uint32_t q2[kRows], k2[kRows];
@@ -263,14 +396,14 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       // channel is at most KDA_MAX_CHUNK_LOG_DECAY
       if (kact && quarter == 0 && fminf(glast.x, glast.y) < -KDA_MAX_CHUNK_LOG_DECAY)
         set_status(P.status, KDA_ERR_GATE_RANGE);
-      // ---- hi buffer c%2 free once the state pass is done with chunk c-2; the
-      // lo area once the inverse of chunk c-1 is done with its scratch
+      // ---- hi buffer c%2 free once the state pass is done with chunk c-2
       if (c >= 2) wait_bar(&bar[bHiFree + (c & 1)], par((c >> 1) - 1), abort_flag, P.status);
-      if (c >= 1) wait_bar(&bar[bLoFree], par(c - 1), abort_flag, P.status);
       if (kact && quarter == 0)
         *reinterpret_cast<float2*>(gam_base + (c & 1) * K + c0) = make_float2(__expf(glast.x), __expf(glast.y));
       uint8_t* hi = sm + Lay::HI + (c & 1) * Lay::kHi;
-      uint32_t kdl[kRows];
+      // gated operands: the hi halves go to their tiles now, the lo halves wait
+      // in registers until the inverse of chunk c-1 has left the lo area
+      uint32_t qgl[kRows], kgl[kRows], kdl[kRows];
       if (kact) {
         f2 G2 = f2_make(G.x, G.y);
         const f2 kLog2e2 = f2_make(1.4426950408889634f, 1.4426950408889634f);
@@ -287,9 +420,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
           const f2 Kg = f2_mul(k, eG);
           const f2 Kd = f2_mul(k, eN);
           const uint32_t swr = uint32_t(rr & 7) << 4, rowr = uint32_t(rr) * 128u;
-          const uint32_t oq = (xA ^ swr) + rowr, ok = oq + 8192u, od = (xB ^ swr) + rowr;
-          *reinterpret_cast<uint32_t*>(lo + oq) = split2(hi + oq, Qg);
-          *reinterpret_cast<uint32_t*>(lo + ok) = split2(hi + ok, Kg);
+          const uint32_t oq = (xA ^ swr) + rowr, od = (xB ^ swr) + rowr;
+          qgl[rr] = split2(hi + oq, Qg);
+          kgl[rr] = split2(hi + oq + 8192u, Kg);
           kdl[rr] = split2(hi + Lay::kA1 + od, Kd);
           if (i < L) {
             const size_t tok = size_t(t0 + i) * P.Hv + hv;
@@ -297,6 +430,16 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
             if constexpr (kQG)
               *reinterpret_cast<uint32_t*>(reinterpret_cast<__nv_bfloat16*>(A.QG) + tok * K + c0) = f2_to_bf16x2(Qg);
           }
+        }
+      }
+      if (c >= 1) wait_bar(&bar[bLoFree], par(c - 1), abort_flag, P.status);
+      __syncwarp();
+      if (kact) {
+#pragma unroll
+        for (int rr = 0; rr < kRows; ++rr) {
+          const uint32_t oq = (xA ^ (uint32_t(rr & 7) << 4)) + uint32_t(rr) * 128u;
+          *reinterpret_cast<uint32_t*>(lo + oq) = qgl[rr];
+          *reinterpret_cast<uint32_t*>(lo + oq + 8192u) = kgl[rr];
         }
       }
       fence_proxy_async_smem();
@@ -316,6 +459,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         for (int at = 0; at < K / 64; ++at) umma_atom4(tmem + kColD1, lo_d + at * 1024, b_hi + at * 512, id, 1);
         umma_commit(&bar[bLoA]);
       }
+      __syncwarp();  // the issuer's warp-mates wait here rather than spin beside it
       // ---- Kd's low half into the area A1_lo used, once hi*hi + lo*hi is done
       wait_bar(&bar[bLoA], par(c), abort_flag, P.status);
       if (kact) {
@@ -331,6 +475,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         for (int at = 0; at < K / 64; ++at) umma_atom4(tmem + kColD1, a_hi + at * 1024, lo_d + at * 512, id, 1);
         umma_commit(&bar[bD1Full]);
       }
+      __syncwarp();
     }
     if (mma_leader) {
       umma_commit(&bar[bDrain]);
@@ -339,6 +484,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
 
   } else if (warp < kWarpState0) {
     // ====================================================== intra epilogue
+    regs_dec<kRegsIntra>();
     const int e = tid - kWarpIntra0 * 32;  // 0..127
     const int q4 = warp & 3;               // TMEM lane quadrant
     const bool akk = q4 >= 2;              // lanes 64-127: Kg rows of D1 (Akk); lanes 0-63: Qg rows (Aqk)
@@ -349,8 +495,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     float* sB = reinterpret_cast<float*>(sm + Lay::BETA);
     uint8_t* wd = sm + Lay::WD;
     uint8_t* vt = sm + Lay::VT;
-    // L2 prefetch of chunk cc's q, k, v, g (one TMA tensor prefetch each), and
-    // the TMA copy of its v rows into the v tile (64-channel boxes, SWIZZLE_128B)
+    // L2 prefetch of chunk cc's q, k, v, g (one TMA tensor prefetch each; the
+    // prep warps prefetch the chunks after the first), and the TMA copy of its
+    // v rows into the v tile (64-channel boxes, SWIZZLE_128B)
     auto prefetch = [&](int cc) {
       const int t = bos + cc * kChunk;
       tma_prefetch_l2_3d(&maps.q, 0, hq, t);
@@ -366,9 +513,11 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     };
     if (leader) {
       prefetch(0);
-      if (nch > 1) prefetch(1);
       load_v(0);
     }
+    // B2's entries above the diagonal are never written: clear the tile once
+    for (int i = e; i < 64 * 64 * 2 / 16; i += 128)
+      reinterpret_cast<uint4*>(sm + Lay::B2)[i] = make_uint4(0u, 0u, 0u, 0u);
     for (int c = 0; c < nch; ++c) {
       const int t0 = bos + c * kChunk, L = min(kChunk, len - c * kChunk);
       const float br = (akk && r < L) ? load_beta(A.beta, P.beta_fp32, size_t(t0 + r) * P.Hv + hv) : 0.f;
@@ -378,8 +527,12 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         uint32_t xa[32], xb[32];
         tmem_ld_x32(tmem_addr(tmem, 32 * q4, kColD1), xa);
         tmem_ld_x32(tmem_addr(tmem, 32 * q4, kColD1 + 32), xb);
-        tc_fence_before();
-        mbar_arrive(&bar[bD1Empty]);
+        // the Aqk rows are read again for their fp32 export after MMA2: only the
+        // Akk half of D1 is released here
+        if (akk) {
+          tc_fence_before();
+          mbar_arrive(&bar[bD1Empty]);
+        }
         if (akk) {
           // row r of A: beta_r Akk[r][i] for i < r, zero elsewhere
           float* arow = Am + r * kLd;
@@ -394,23 +547,16 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
           sB[r] = br;
         } else {
           // Aqk row r (causal mask): bf16 operand tile of O^T += Delta^T Aqk^T
-          // (without scale: the state pass multiplies O by scale at the end)
-          // and the fp32 export with scale; the tile of chunk c-2 must be done
+          // (without scale: the state pass multiplies O by scale at the end);
+          // the tile of chunk c-2 must be done
           if (c >= 2) wait_bar(&bar[bHiFree + (c & 1)], par((c >> 1) - 1), abort_flag, P.status);
           uint8_t* aqkb = sm + Lay::AQKB + (c & 1) * 8192;
-          float* arow = A.Aqk ? A.Aqk + (size_t(t0 + r) * P.Hv + hv) * 64 : nullptr;
 #pragma unroll
           for (int i = 0; i < 64; i += 8) {
             float f[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) f[j] = (i + j <= r) ? __uint_as_float(i + j < 32 ? xa[i + j] : xb[i + j - 32]) : 0.f;
             *reinterpret_cast<uint4*>(aqkb + sw128_offset(uint32_t(r), uint32_t(i), 64)) = pack8(f);
-            if (arow && r < L) {
-              *reinterpret_cast<float4*>(arow + i) =
-                  make_float4(P.scale * f[0], P.scale * f[1], P.scale * f[2], P.scale * f[3]);
-              *reinterpret_cast<float4*>(arow + i + 4) =
-                  make_float4(P.scale * f[4], P.scale * f[5], P.scale * f[6], P.scale * f[7]);
-            }
           }
           fence_proxy_async_smem();
         }
@@ -428,53 +574,54 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
           for (int i = 0; i < rr; ++i) acc = fmaf(Am[(base + rr) * kLd + base + i], x[i], acc);
           x[rr] = (rr == cc ? 1.f : 0.f) - acc;
         }
+        uint8_t* b2 = sm + Lay::B2;
+        const float bc = sB[base + cc];
 #pragma unroll
-        for (int rr = 0; rr < 16; ++rr) Xm[(base + rr) * kLd + base + cc] = x[rr];
-      }
-      named_bar_sync(kNbIntra, 128);
-      // 32 x 32 diagonal blocks: X_10 = -X_11 (A_10 X_00) and X_32 = -X_33 (A_32 X_22).
-      // Thread = (half b, row, column quad); T goes into the dead block A_00 / A_22.
-      {
-        const int b = e >> 6, row = (e >> 2) & 15, c4 = 4 * (e & 3);
-        const int ro = b ? 48 : 16, co = b ? 32 : 0;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-        for (int kk = c4; kk < 16; ++kk)
-          acc = fma4(Am[(ro + row) * kLd + co + kk], *reinterpret_cast<const float4*>(Xm + (co + kk) * kLd + co + c4), acc);
-        *reinterpret_cast<float4*>(Am + (co + row) * kLd + co + c4) = acc;
-        named_bar_sync(kNbIntra, 128);
-        float4 xs = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-        for (int m = 0; m <= row; ++m)
-          xs = fma4(Xm[(ro + row) * kLd + ro + m], *reinterpret_cast<const float4*>(Am + (co + m) * kLd + co + c4), xs);
-        *reinterpret_cast<float4*>(Xm + (ro + row) * kLd + co + c4) = make_float4(-xs.x, -xs.y, -xs.z, -xs.w);
-      }
-      named_bar_sync(kNbIntra, 128);
-      // the lower-left 32 x 32 block: X_BL = -X_BR (A_BL X_TL).  Thread = (row,
-      // column octet); T goes into the dead top-left block of A.
-      {
-        const int row = e >> 2, c8 = 8 * (e & 3);
-        float4 t0v = make_float4(0.f, 0.f, 0.f, 0.f), t1v = t0v;
-#pragma unroll 4
-        for (int kk = c8; kk < 32; ++kk) {
-          const float a = Am[(32 + row) * kLd + kk];
-          t0v = fma4(a, *reinterpret_cast<const float4*>(Xm + kk * kLd + c8), t0v);
-          t1v = fma4(a, *reinterpret_cast<const float4*>(Xm + kk * kLd + c8 + 4), t1v);
+        for (int rr = 0; rr < 16; ++rr) {
+          Xm[(base + rr) * kLd + base + cc] = x[rr];
+          *reinterpret_cast<__nv_bfloat16*>(b2 + sw128_offset(uint32_t(base + rr), uint32_t(base + cc), 64)) =
+              __float2bfloat16_rn(x[rr] * bc);
         }
-        *reinterpret_cast<float4*>(Am + row * kLd + c8) = t0v;
-        *reinterpret_cast<float4*>(Am + row * kLd + c8 + 4) = t1v;
-        named_bar_sync(kNbIntra, 128);
-        float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
-#pragma unroll 4
-        for (int m = 0; m <= row; ++m) {
-          const float xv = Xm[(32 + row) * kLd + 32 + m];
-          x0 = fma4(xv, *reinterpret_cast<const float4*>(Am + m * kLd + c8), x0);
-          x1 = fma4(xv, *reinterpret_cast<const float4*>(Am + m * kLd + c8 + 4), x1);
-        }
-        *reinterpret_cast<float4*>(Xm + (32 + row) * kLd + c8) = make_float4(-x0.x, -x0.y, -x0.z, -x0.w);
-        *reinterpret_cast<float4*>(Xm + (32 + row) * kLd + c8 + 4) = make_float4(-x1.x, -x1.y, -x1.z, -x1.w);
       }
       named_bar_sync(kNbIntra, 128);
+      // The off-diagonal blocks on the warps' tensor cores (mma.m16n8k8 on
+      // TF32 hi/lo pairs, fp32-accurate); each X block goes to the fp32 scratch
+      // and, times beta of its columns, to the bf16 B2 tile (whose entries
+      // above the diagonal are never written: zero since the kernel began).
+      // 32 x 32 diagonal blocks first: X_10 = -X_11 (A_10 X_00) and
+      // X_32 = -X_33 (A_32 X_22), T in the dead diagonal blocks A_00 / A_22;
+      // warps 0, 1 the top block's column halves, warps 2, 3 the bottom's.
+      uint8_t* b2 = sm + Lay::B2;
+      {
+        const int iw = warp - kWarpIntra0;
+        const int co = (iw >> 1) ? 32 : 0, ro = co + 16, nb = 8 * (iw & 1);
+        float d[4];
+        mma_3xtf32_x1(d, Am + ro * kLd + co, kLd, Xm + co * kLd + co + nb, kLd, 0, 16);
+        store_frag(Am + co * kLd + co + nb, kLd, d, 1.f);
+        __syncwarp();  // the second product reads only the T columns this warp wrote
+        float x[4];
+        mma_3xtf32_x1(x, Xm + ro * kLd + ro, kLd, Am + co * kLd + co + nb, kLd, 0, 16);
+        store_x_b2(Xm, b2, sB, ro, co + nb, x, -1.f);
+      }
+      named_bar_sync(kNbIntra, 128);
+      // the lower-left 32 x 32 block: X_BL = -X_BR (A_BL X_TL), T_BL in the dead
+      // top-left block of A.  Warp iw owns rows 16 (iw >> 1) .. + 15 and
+      // columns 16 (iw & 1) .. + 15.  The blocks of X never written (above the
+      // diagonal blocks) are skipped: X_TL's columns 16-31 take only the terms
+      // 16-31, X_BR's rows 32-47 only the terms 32-47.
+      {
+        const int iw = warp - kWarpIntra0;
+        const int mt = 16 * (iw >> 1), nt = 16 * (iw & 1);
+        float d0[4], d1[4];
+        mma_3xtf32_x2(d0, d1, Am + (32 + mt) * kLd, kLd, Xm + nt, kLd, nt, 32);
+        store_frag(Am + mt * kLd + nt, kLd, d0, 1.f);
+        store_frag(Am + mt * kLd + nt + 8, kLd, d1, 1.f);
+        named_bar_sync(kNbIntra, 128);
+        float x0[4], x1[4];
+        mma_3xtf32_x2(x0, x1, Xm + (32 + mt) * kLd + 32, kLd, Am + nt, kLd, 0, mt + 16);
+        store_x_b2(Xm, b2, sB, 32 + mt, nt, x0, -1.f);
+        store_x_b2(Xm, b2, sB, 32 + mt, nt + 8, x1, -1.f);
+      }
       // ---- v of this chunk: a tail chunk's rows past its end hold tokens of
       // the next chunk or sequence; clear them so that U depends on this
       // chunk's tokens alone
@@ -484,20 +631,6 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         for (int a = 0; a < V / 64; ++a)
           for (int i = e; i < pieces; i += 128)
             *reinterpret_cast<uint4*>(vt + a * 8192 + (L + (i >> 3)) * 128 + (i & 7) * 16) = make_uint4(0, 0, 0, 0);
-      }
-      // ---- B2 = X diag(beta) (bf16, K-major rows r); B2 of chunk c-1 was read
-      // by MMA2(c-1), whose completion these threads saw before its W tile
-      {
-        const int rr = e >> 1, c32 = 32 * (e & 1);
-        uint8_t* b2 = sm + Lay::B2;
-#pragma unroll
-        for (int j = 0; j < 32; j += 8) {
-          const int col = c32 + j;
-          float f[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) f[i] = (col + i <= rr) ? Xm[rr * kLd + col + i] * sB[col + i] : 0.f;
-          *reinterpret_cast<uint4*>(b2 + sw128_offset(uint32_t(rr), uint32_t(col), 64)) = pack8(f);
-        }
       }
       fence_proxy_async_smem();
       named_bar_sync(kNbIntra, 128);
@@ -519,7 +652,11 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         umma_commit(&bar[bD2Full]);
       }
       __syncwarp();
-      // ---- Akk_inv export by whole rows (8 passes of 8 rows x 16 column quads)
+      // ---- exports after MMA2: Akk_inv by whole rows from the scratch (8
+      // passes of 8 rows x 16 column quads, all 128 threads), then the lo area
+      // is free; then the Aqk warps read their rows of D1 again (releasing it)
+      // and write Aqk (scaled, causal mask), 32 bytes a store when the output
+      // is 32-byte aligned
       if (A.Akk_inv) {
 #pragma unroll 2
         for (int it = 0; it < 8; ++it) {
@@ -533,55 +670,32 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         }
       }
       mbar_arrive(&bar[bLoFree]);
-      // ---- W^T (lane = channel k) into the W tile of the state pass (MN-major:
-      // row k holds its 64 tokens) and the W / U exports (thread = channel)
+      if (!akk) {
+        float* arow = A.Aqk + (size_t(t0 + r) * P.Hv + hv) * 64;
+        const bool wr = A.Aqk && r < L;
+        uint32_t x[64];
+        tmem_ld_x64(tmem_addr(tmem, 32 * q4, kColD1), x);
+        tc_fence_before();
+        mbar_arrive(&bar[bD1Empty]);
+        if (wr) {
+#pragma unroll
+          for (int i = 0; i < 64; i += 8) {
+            float f[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) f[j] = (i + j <= r) ? P.scale * __uint_as_float(x[i + j]) : 0.f;
+            const float4 lo4 = make_float4(f[0], f[1], f[2], f[3]), hi4 = make_float4(f[4], f[5], f[6], f[7]);
+            if (A.aqk_v8) {
+              st_global_v8(arow + i, lo4, hi4);  // a whole 32-byte sector per thread
+            } else {
+              *reinterpret_cast<float4*>(arow + i) = lo4;
+              *reinterpret_cast<float4*>(arow + i + 4) = hi4;
+            }
+          }
+        }
+      }
+      // ---- MMA2 is done with the v tile: copy the next chunk's v
       wait_bar(&bar[bD2Full], par(c), abort_flag, P.status);
-      if (leader) {
-        // MMA2 is done with the v tile: copy the next chunk's v, prefetch the one after
-        if (c + 1 < nch) load_v(c + 1);
-        if (c + 2 < nch) prefetch(c + 2);
-      }
-      if (c >= 1) wait_bar(&bar[bHODone], par(c - 1), abort_flag, P.status);  // Delta^T(c-1) consumed
-      tc_fence_after();
-      {
-        const int ch = 32 * q4 + lane;
-        uint32_t w[32];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          tmem_ld_x32(tmem_addr(tmem, 32 * q4, kColW + 32 * h), w);
-          if (ch < K) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              float f[8];
-#pragma unroll
-              for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(w[8 * j + i]);
-              *reinterpret_cast<uint4*>(wd + ch * 128 + ((uint32_t(4 * h + j) ^ uint32_t(ch & 7)) << 4)) = pack8(f);
-            }
-            if (A.W) {
-              __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(A.W) + (size_t(t0 + 32 * h) * P.Hv + hv) * K + ch;
-#pragma unroll
-              for (int t = 0; t < 32; ++t)
-                if (32 * h + t < L) dst[size_t(t) * P.Hv * K] = __float2bfloat16_rn(__uint_as_float(w[t]));
-            }
-          }
-        }
-        if (A.U) {
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            tmem_ld_x32(tmem_addr(tmem, 32 * q4, kColU + 32 * h), w);
-            if (ch < V) {
-              __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(A.U) + (size_t(t0 + 32 * h) * P.Hv + hv) * V + ch;
-#pragma unroll
-              for (int t = 0; t < 32; ++t)
-                if (32 * h + t < L) dst[size_t(t) * P.Hv * V] = __float2bfloat16_rn(__uint_as_float(w[t]));
-            }
-          }
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(&bar[bD2Empty]);
-      fence_proxy_async_smem();
-      mbar_arrive(&bar[bWFull]);
+      if (leader && c + 1 < nch) load_v(c + 1);
     }
     if (leader) {
       // after an abort: the last v copy and the last MMA2 must land before exit
@@ -592,6 +706,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
 
   } else {
     // =============================================================== state
+    regs_dec<kRegsState>();
     const int q4 = warp & 3;
     const int v = 32 * q4 + lane;  // value channel = TMEM lane
     const bool vv = v < V;
@@ -642,10 +757,33 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       const int L = min(kChunk, len - c * kChunk);
       const uint32_t hi_addr = smem_u32(sm + Lay::HI + (c & 1) * Lay::kHi);
       const uint32_t ocol = kColO + 64 * (c & 1);
+      // W^T (TMEM lane = channel k) into the W tile, MN-major: row k holds its
+      // 64 tokens.  The tile's previous reader, the H MMA of chunk c-1, is done.
+      // MMA2 commits after the Aqk_b tile of chunk c was written (its issuer
+      // waits for the intra warps first), so D2 full also covers that tile.
+      wait_bar(&bar[bD2Full], par(c), abort_flag, P.status);
+      tc_fence_after();
+      const int t0 = bos + c * kChunk;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t w[32];
+        tmem_ld_x32(lane_base + kColW + 32 * h, w);
+        if (v < K) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            float f[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(w[8 * j + i]);
+            *reinterpret_cast<uint4*>(wd + v * 128 + ((uint32_t(4 * h + j) ^ uint32_t(v & 7)) << 4)) = pack8(f);
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      named_bar_sync(kNbState, 128);
       if (leader) {
         // P^T = S^T W^T (W tile MN-major: a K step of 16 channels is 2048 B), then
         // O^T = S^T Qg^T (Qg rows 0-63 of A1_hi, K-major)
-        wait_bar(&bar[bWFull], par(c), abort_flag, P.status);
         tc_fence_after();
         constexpr uint32_t idP = idesc_bf16_f32(128, 64) | kIdescBMajorMN;
         constexpr uint32_t id64 = idesc_bf16_f32(128, 64);
@@ -659,8 +797,21 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         for (int g = 0; g < K / 64; ++g) umma_atom4(tmem + ocol, a_st + g * 1024, b_qg + g * 1024, id64, g > 0);
       }
       __syncwarp();
+      // exports while P runs: W of this chunk (thread = channel k), o of the last
+      if (A.W) {
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {
+          uint32_t w[32];
+          tmem_ld_x32(lane_base + kColW + 32 * h, w);  // W^T again: D2 stays valid until this chunk's Delta
+          if (v < K) {
+            __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(A.W) + (size_t(t0 + 32 * h) * P.Hv + hv) * K + v;
+#pragma unroll
+            for (int t = 0; t < 32; ++t)
+              if (32 * h + t < L) dst[size_t(t) * P.Hv * K] = __float2bfloat16_rn(__uint_as_float(w[t]));
+          }
+        }
+      }
       if (c >= 1) read_o(c - 1);
-      wait_bar(&bar[bD2Full], par(c), abort_flag, P.status);
       wait_bar(&bar[bPDone], par(c), abort_flag, P.status);
       tc_fence_after();
       // Delta^T row v: U^T - P^T, tokens past the chunk's end zero (into the W
@@ -677,6 +828,12 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
           for (int i = 0; i < 8; ++i)
             d[i] = (vv && 32 * h + j + i < L) ? __uint_as_float(ur[j + i]) - __uint_as_float(pr[j + i]) : 0.f;
           *reinterpret_cast<uint4*>(wd + v * 128 + ((uint32_t((32 * h + j) >> 3) ^ uint32_t(v & 7)) << 4)) = pack8(d);
+        }
+        if (A.U && vv) {
+          __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(A.U) + (size_t(t0 + 32 * h) * P.Hv + hv) * V + v;
+#pragma unroll
+          for (int t = 0; t < 32; ++t)
+            if (32 * h + t < L) dst[size_t(t) * P.Hv * V] = __float2bfloat16_rn(__uint_as_float(ur[t]));
         }
       }
       tc_fence_before();
@@ -720,7 +877,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&bar[bHiFree + (c & 1)]);
-      named_bar_sync(kNbState, 128);
+      // (the next chunk's barrier after its W tile also orders these S^T writes
+      // before its P MMA)
     }
     read_o(nch - 1);
     if (A.hT) {

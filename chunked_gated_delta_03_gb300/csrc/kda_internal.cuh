@@ -13,6 +13,7 @@ namespace kda {
 
 constexpr int kChunk = 64;                          // rows per chunk
 constexpr uint64_t kWaitLimitNs = 2000000000ull;    // bounded waits: 2 s
+constexpr uint32_t kWaitBackoffMaxNs = 64;          // longest sleep between polls of a wait
 constexpr int kMaxDevicesCached = 64;               // per-device caches of launch attributes
 
 // Sizes and chunk bookkeeping of one call, passed by value to every kernel.
@@ -79,9 +80,10 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
 #pragma unroll 1
     for (int i = 0; i < 4; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    // back off so that waiting warps leave issue slots to working ones
+    // back off so that waiting warps leave issue slots to working ones, but
+    // briefly: a hand-off on a critical path should wake its waiter promptly
     __nanosleep(sleep_ns);
-    if (sleep_ns < 256) sleep_ns *= 2;
+    if (sleep_ns < kWaitBackoffMaxNs) sleep_ns *= 2;
     if (*abort_flag) return false;
     if (globaltimer_ns() - t0 > kWaitLimitNs) {
       *abort_flag = 1;
@@ -154,6 +156,7 @@ struct FusedArgs {
   void* U;                  // bf16 [BT, Hv, V] or null
   float* G;                 // fp32 [BT, Hv, K] or null
   void* QG;                 // bf16 [BT, Hv, K] or null
+  int aqk_v8;               // Aqk is 32-byte aligned: its rows are written with 32-byte stores
 };
 
 cudaError_t launch_chunk_index(const int32_t* cu, int N, int T, int chunk, int32_t* idx, int32_t* off,

@@ -318,9 +318,22 @@ int two_pass_forward(const Shape& s, const KdaArgs* a, uint8_t* ws, const Layout
 int fused_forward(const Shape& s, const KdaArgs* a, uint8_t* ws, const Layout& L, const DeviceInfo& d,
                   cudaEvent_t const* ev, cudaStream_t st) {
   const Problem P = make_problem(s, a, ws, L);
-  IntraMaps m;
-  if (!make_intra_maps(s, a, &m)) return KDA_ERR_LAUNCH;
+  IntraMaps im;
+  if (!make_intra_maps(s, a, &im)) return KDA_ERR_LAUNCH;
+  FusedMaps m;
+  m.q = im.q;
+  m.k = im.k;
+  m.v = im.v;
+  m.g = im.g;
+  m.v_sw = im.v_sw;
   FusedArgs f{};
+  // outputs whose base and strides a TMA store map accepts (16-byte alignment)
+  // leave by TMA stores of whole chunks; the others by per-thread stores
+  const auto bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
+  f.o_tma = aligned16(a->o) && map_tokens(&m.o, a->o, bf, 2, s.V, s.Hv, s.BT, 64, sw);
+  f.w_tma = a->W && aligned16(a->W) && map_tokens(&m.W, a->W, bf, 2, s.K, s.Hv, s.BT, 64, sw);
+  f.u_tma = a->U && aligned16(a->U) && map_tokens(&m.U, a->U, bf, 2, s.V, s.Hv, s.BT, 64, sw);
   f.q = a->q;
   f.k = a->k;
   f.g = a->g;

@@ -53,29 +53,26 @@ constexpr uint32_t kNbPrep = 1, kNbIntra = 2, kNbState = 3;  // named barriers
 
 // TMEM columns
 constexpr uint32_t kColD1 = 0;     // MMA1: lanes 0-63 Aqk / scale, 64-127 Akk / beta (64 cols)
-constexpr uint32_t kColW = 64;     // MMA2: W^T, lane = channel k (64 cols = tokens)
+constexpr uint32_t kColW = 64;     // MMA2: W^T, lane = channel k (64 cols = tokens); then P^T = S^T W^T, lane = v
 constexpr uint32_t kColU = 128;    // MMA2: U^T, lane = channel v
-constexpr uint32_t kColP = 192;    // P^T = S^T W^T, lane = v
-constexpr uint32_t kColO = 256;    // O^T, two buffers (256, 320), lane = v
+constexpr uint32_t kColDt = 192;   // Delta^T in bf16 pairs (32 cols = 64 tokens): A operand of the state MMAs
+constexpr uint32_t kColO = 256;    // O^T, lane = v
+constexpr uint32_t kColSb = 320;   // S^T in bf16 pairs (K / 2 cols): A operand of P^T and O^T
 constexpr uint32_t kColS = 384;    // S^T in fp32, lane = v, column = k
-
-__host__ __device__ constexpr uint32_t round1k(uint32_t x) { return (x + 1023u) / 1024u * 1024u; }
 
 template <int K, int V>
 struct FusedLayout {
   static constexpr uint32_t kA1 = K * 256;  // [Qg; Kg]: K/64 atoms of 128 rows x 128 B
   static constexpr uint32_t kB1 = K * 128;  // Kd: K/64 atoms of 64 rows x 128 B
   static constexpr uint32_t kHi = kA1 + kB1;
-  static constexpr uint32_t kScratch = 2 * 64 * kLd * 4;  // fp32 A and X of the inverse
-  static constexpr uint32_t kLo = round1k(kA1 > kScratch ? kA1 : kScratch);
   static constexpr uint32_t HI = 0;                        // 2 x (A1_hi, B1_hi)
-  static constexpr uint32_t LO = HI + 2 * kHi;             // A1_lo, then Kd_lo, then the inverse scratch
-  static constexpr uint32_t VT = LO + kLo;                 // v: 64 token rows, 64-channel blocks 8 KB apart
-  static constexpr uint32_t AQKB = VT + 16384;             // 2 x Aqk / scale, bf16 64 x 64, K-major
+  static constexpr uint32_t LO = HI + 2 * kHi;             // A1_lo, then Kd_lo
+  static constexpr uint32_t VT = LO + kA1;                 // v: 64 token rows, 64-channel blocks 8 KB apart
+  static constexpr uint32_t AQKB = VT + V * 128;           // 2 x Aqk / scale, bf16 64 x 64, K-major
   static constexpr uint32_t B2 = AQKB + 2 * 8192;          // X diag(beta), bf16 64 x 64, K-major
-  static constexpr uint32_t ST = B2 + 8192;                // S^T bf16: K/64 atoms of 128 rows x 128 B
-  static constexpr uint32_t WD = ST + K * 256;             // W tile (K rows of 64 tokens) / Delta^T (128 rows)
-  static constexpr uint32_t GAM = WD + 16384;              // 2 x K floats: gamma
+  static constexpr uint32_t UST = B2 + 8192;               // U staged token-major for its TMA store
+  static constexpr uint32_t SCR = UST + V * 128;           // fp32 A and X of the inverse, 64 x kLd each
+  static constexpr uint32_t GAM = SCR + 2 * 64 * kLd * 4;  // 2 x K floats: gamma
   static constexpr uint32_t BETA = GAM + 2 * K * 4;        // 64 floats
   static constexpr uint32_t PART = BETA + 64 * 4;          // 2 x 4 x K floats: cumsum partial sums
   static constexpr uint32_t BARS = PART + 2 * 4 * K * 4;
@@ -84,34 +81,32 @@ struct FusedLayout {
   static constexpr uint32_t ABORT = TMEM_SLOT + 4;
   static constexpr uint32_t total = ABORT + 4;
   static constexpr uint32_t bytes = total + 1024;  // slack for the 1024-B alignment of the base
-  static_assert(LO % 1024 == 0 && VT % 1024 == 0 && AQKB % 1024 == 0 && B2 % 1024 == 0 && ST % 1024 == 0 &&
-                    WD % 1024 == 0,
-                "operand tiles must be 1024-B aligned");
+  static_assert(LO % 1024 == 0 && VT % 1024 == 0 && AQKB % 1024 == 0 && B2 % 1024 == 0 && UST % 1024 == 0,
+                "operand and staging tiles must be 1024-B aligned");
   static_assert(bytes <= 227 * 1024, "shared memory budget");
 };
 
 // barrier indices
 enum {
   bLoA = 0,      // MMA1 hi*hi + lo*hi done: A1_lo may be overwritten            (commit)
-  bD1Full = 1,   // MMA1 done -> intra epilogue                                  (commit)
+  bD1Full = 1,   // MMA1 done -> intra epilogue; the lo area is free again       (commit)
   bD1Empty = 2,  // intra epilogue read D1 -> MMA1                               (128)
-  bLoFree = 3,   // intra epilogue done with the scratch in the lo area -> prep  (128)
-  bHiFree = 4,   // [2] state done with hi buffer b (and its gamma) -> prep, Aqk (128)
+  bHiFree = 4,   // [2] state done with hi buffer b (and its gamma, Aqk tile)    (128)
   bVFull = 6,    // TMA: v chunk landed                                          (1 + bytes)
   bD2Full = 7,   // MMA2 done (after Aqk_b was written) -> intra epilogue, state (commit)
-  bD2Empty = 8,  // state read W^T / U^T -> MMA2                                (128)
-  bPDone = 10,   // P^T and O^T = S^T Qg^T done -> state                         (commit)
-  bHODone = 11,  // S^T += Delta^T Kd and O^T += Delta^T Aqk^T done              (commit)
+  bD2Empty = 8,  // state read W^T / U^T / P^T -> MMA2                           (128)
+  bPDone = 10,   // P^T = S^T W^T done -> state                                  (commit)
+  bHODone = 11,  // S^T += Delta^T Kd and O^T (both parts) done                  (commit)
   bDrain = 12,   // [3] final drains of the three MMA issuers                    (commit)
 };
 
 __device__ __forceinline__ uint32_t par(int n) { return uint32_t(n) & 1u; }
 
 // Register budgets per warpgroup (setmaxnreg; the kernel launches with 128 a
-// thread, 65536 in all): the prep warpgroups take 160, the intra warpgroup
-// 104, the state warpgroup 88 -- 2 x 128 x 160 + 128 x 104 + 128 x 88 = 65536,
-// so the increase never waits for registers that are not there.
-constexpr uint32_t kRegsPrep = 160, kRegsIntra = 104, kRegsState = 88;
+// thread, 65536 in all): the prep warpgroups take 144, the intra and state
+// warpgroups 112 each -- 2 x 128 x 144 + 2 x 128 x 112 = 65536, so the
+// increase never waits for registers that are not there.
+constexpr uint32_t kRegsPrep = 144, kRegsIntra = 112, kRegsState = 112;
 static_assert(2 * 128 * kRegsPrep + 128 * kRegsIntra + 128 * kRegsState <= 65536, "register split");
 template <uint32_t N>
 __device__ __forceinline__ void regs_inc() {
@@ -128,12 +123,11 @@ __device__ __forceinline__ float exp2f_fast(float x) {
   return y;
 }
 
-// x = hi + lo with hi = bf16(x), lo = bf16(x - hi), on a channel pair: stores
-// hi at hi_p, returns lo (both as bf16x2).
-__device__ __forceinline__ uint32_t split2(uint8_t* hi_p, f2 x) {
-  const uint32_t h = f2_to_bf16x2(x);
-  *reinterpret_cast<uint32_t*>(hi_p) = h;
-  return f2_to_bf16x2(f2_sub(x, f2_from_bf16x2(h)));
+// x = hi + lo with hi = bf16(x), lo = bf16(x - hi), on a channel pair (both
+// as bf16x2): sets hi, returns lo.
+__device__ __forceinline__ uint32_t split2(uint32_t& hi, f2 x) {
+  hi = f2_to_bf16x2(x);
+  return f2_to_bf16x2(f2_sub(x, f2_from_bf16x2(hi)));
 }
 
 __device__ __forceinline__ uint4 pack8(const float* f) {
@@ -144,14 +138,6 @@ __device__ __forceinline__ uint4 pack8(const float* f) {
 __device__ __forceinline__ float load_beta(const void* beta, int fp32, size_t i) {
   return fp32 ? __ldg(reinterpret_cast<const float*>(beta) + i)
               : __bfloat162float(__ldg(reinterpret_cast<const __nv_bfloat16*>(beta) + i));
-}
-
-__device__ __forceinline__ float4 fma4(float a, float4 x, float4 acc) {
-  acc.x = fmaf(a, x.x, acc.x);
-  acc.y = fmaf(a, x.y, acc.y);
-  acc.z = fmaf(a, x.z, acc.z);
-  acc.w = fmaf(a, x.w, acc.w);
-  return acc;
 }
 
 // fp32 x -> (hi, lo) TF32 bit patterns with x ~ hi + lo: hi rounded to nearest
@@ -265,7 +251,7 @@ __device__ __forceinline__ void store_frag(float* C, int ldc, const float (&d)[4
 
 template <int K, int V, bool kQG>
 __global__ void __launch_bounds__(kFusedThreads, 1)
-    fused_kernel(const Problem P, const FusedArgs A, const __grid_constant__ IntraMaps maps) {
+    fused_kernel(const Problem P, const FusedArgs A, const __grid_constant__ FusedMaps maps) {
   using Lay = FusedLayout<K, V>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -303,7 +289,6 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     mbar_init(&bar[bLoA], 1);
     mbar_init(&bar[bD1Full], 1);
     mbar_init(&bar[bD1Empty], 128);
-    mbar_init(&bar[bLoFree], 128);
     mbar_init(&bar[bHiFree], 128);
     mbar_init(&bar[bHiFree + 1], 128);
     mbar_init(&bar[bVFull], 1);
@@ -343,12 +328,13 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     uint8_t* lo = sm + Lay::LO;
     for (int c = 0; c < nch; ++c) {
       const int t0 = bos + c * kChunk, L = min(kChunk, len - c * kChunk);
-      // ---- L2 prefetch of the next chunk's q, k, v and g (a box of 64 token
-      // rows of one head each, one per thread of lanes 0 of warps 0-3), a whole
-      // chunk period ahead of its loads
-      if (lane == 0 && warp < 4 && c + 1 < nch) {
+      // ---- L2 prefetch of the next chunk's q, k and g (a box of 64 token rows
+      // of one head each, one per thread of lanes 0 of warps 0-2), a whole
+      // chunk period ahead of its loads.  (v needs none: its TMA copy is
+      // issued as soon as the previous chunk's MMA2 is done.)
+      if (lane == 0 && warp < 3 && c + 1 < nch) {
         const int tn = t0 + kChunk;
-        const CUtensorMap* m = warp == 0 ? &maps.q : warp == 1 ? &maps.k : warp == 2 ? &maps.v : &maps.g;
+        const CUtensorMap* m = warp == 0 ? &maps.q : warp == 1 ? &maps.k : &maps.g;
         tma_prefetch_l2_3d(m, 0, warp < 2 ? hq : hv, tn);
       }
       // ---- loads (all in flight together)
@@ -396,14 +382,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       // channel is at most KDA_MAX_CHUNK_LOG_DECAY
       if (kact && quarter == 0 && fminf(glast.x, glast.y) < -KDA_MAX_CHUNK_LOG_DECAY)
         set_status(P.status, KDA_ERR_GATE_RANGE);
-      // ---- hi buffer c%2 free once the state pass is done with chunk c-2
-      if (c >= 2) wait_bar(&bar[bHiFree + (c & 1)], par((c >> 1) - 1), abort_flag, P.status);
-      if (kact && quarter == 0)
-        *reinterpret_cast<float2*>(gam_base + (c & 1) * K + c0) = make_float2(__expf(glast.x), __expf(glast.y));
-      uint8_t* hi = sm + Lay::HI + (c & 1) * Lay::kHi;
-      // gated operands: the hi halves go to their tiles now, the lo halves wait
-      // in registers until the inverse of chunk c-1 has left the lo area
-      uint32_t qgl[kRows], kgl[kRows], kdl[kRows];
+      // gated operands, all in registers before the waits: hi halves to the hi
+      // tiles, lo halves to the lo area
+      uint32_t qgh[kRows], kgh[kRows], kdh[kRows], qgl[kRows], kgl[kRows], kdl[kRows];
       if (kact) {
         f2 G2 = f2_make(G.x, G.y);
         const f2 kLog2e2 = f2_make(1.4426950408889634f, 1.4426950408889634f);
@@ -419,25 +400,33 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
           const f2 Qg = f2_mul(q, eG);
           const f2 Kg = f2_mul(k, eG);
           const f2 Kd = f2_mul(k, eN);
-          const uint32_t swr = uint32_t(rr & 7) << 4, rowr = uint32_t(rr) * 128u;
-          const uint32_t oq = (xA ^ swr) + rowr, od = (xB ^ swr) + rowr;
-          qgl[rr] = split2(hi + oq, Qg);
-          kgl[rr] = split2(hi + oq + 8192u, Kg);
-          kdl[rr] = split2(hi + Lay::kA1 + od, Kd);
+          qgl[rr] = split2(qgh[rr], Qg);
+          kgl[rr] = split2(kgh[rr], Kg);
+          kdl[rr] = split2(kdh[rr], Kd);
           if (i < L) {
             const size_t tok = size_t(t0 + i) * P.Hv + hv;
             if (A.G) *reinterpret_cast<float2*>(A.G + tok * K + c0) = f2_split(G2);
             if constexpr (kQG)
-              *reinterpret_cast<uint32_t*>(reinterpret_cast<__nv_bfloat16*>(A.QG) + tok * K + c0) = f2_to_bf16x2(Qg);
+              *reinterpret_cast<uint32_t*>(reinterpret_cast<__nv_bfloat16*>(A.QG) + tok * K + c0) = qgh[rr];
           }
         }
       }
-      if (c >= 1) wait_bar(&bar[bLoFree], par(c - 1), abort_flag, P.status);
+      // ---- hi buffer c%2 free once the state pass is done with chunk c-2; the
+      // lo area once MMA1 of chunk c-1 is done
+      if (c >= 2) wait_bar(&bar[bHiFree + (c & 1)], par((c >> 1) - 1), abort_flag, P.status);
+      if (c >= 1) wait_bar(&bar[bD1Full], par(c - 1), abort_flag, P.status);
       __syncwarp();
+      uint8_t* hi = sm + Lay::HI + (c & 1) * Lay::kHi;
       if (kact) {
+        if (quarter == 0)
+          *reinterpret_cast<float2*>(gam_base + (c & 1) * K + c0) = make_float2(__expf(glast.x), __expf(glast.y));
 #pragma unroll
         for (int rr = 0; rr < kRows; ++rr) {
-          const uint32_t oq = (xA ^ (uint32_t(rr & 7) << 4)) + uint32_t(rr) * 128u;
+          const uint32_t swr = uint32_t(rr & 7) << 4, rowr = uint32_t(rr) * 128u;
+          const uint32_t oq = (xA ^ swr) + rowr, od = (xB ^ swr) + rowr;
+          *reinterpret_cast<uint32_t*>(hi + oq) = qgh[rr];
+          *reinterpret_cast<uint32_t*>(hi + oq + 8192u) = kgh[rr];
+          *reinterpret_cast<uint32_t*>(hi + Lay::kA1 + od) = kdh[rr];
           *reinterpret_cast<uint32_t*>(lo + oq) = qgl[rr];
           *reinterpret_cast<uint32_t*>(lo + oq + 8192u) = kgl[rr];
         }
@@ -490,10 +479,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     const bool akk = q4 >= 2;              // lanes 64-127: Kg rows of D1 (Akk); lanes 0-63: Qg rows (Aqk)
     const int r = 32 * (q4 & 1) + lane;    // row of the 64 x 64 matrix
     const bool leader = warp == kWarpIntra0 && lane == 0;
-    float* Am = reinterpret_cast<float*>(sm + Lay::LO);  // A = Akk (beta-scaled, strictly lower), fp32 64 x kLd
+    float* Am = reinterpret_cast<float*>(sm + Lay::SCR);  // A = Akk (beta-scaled, strictly lower), fp32 64 x kLd
     float* Xm = Am + 64 * kLd;                            // X = (I + A)^-1
     float* sB = reinterpret_cast<float*>(sm + Lay::BETA);
-    uint8_t* wd = sm + Lay::WD;
     uint8_t* vt = sm + Lay::VT;
     // L2 prefetch of chunk cc's q, k, v, g (one TMA tensor prefetch each; the
     // prep warps prefetch the chunks after the first), and the TMA copy of its
@@ -523,64 +511,78 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       const float br = (akk && r < L) ? load_beta(A.beta, P.beta_fp32, size_t(t0 + r) * P.Hv + hv) : 0.f;
       wait_bar(&bar[bD1Full], par(c), abort_flag, P.status);
       tc_fence_after();
-      {
-        uint32_t xa[32], xb[32];
-        tmem_ld_x32(tmem_addr(tmem, 32 * q4, kColD1), xa);
-        tmem_ld_x32(tmem_addr(tmem, 32 * q4, kColD1 + 32), xb);
-        // the Aqk rows are read again for their fp32 export after MMA2: only the
-        // Akk half of D1 is released here
-        if (akk) {
-          tc_fence_before();
-          mbar_arrive(&bar[bD1Empty]);
+      // the whole row r of D1 (Aqk / scale or Akk / beta) into registers; D1
+      // is then free for the next chunk's MMA1
+      uint32_t x[64];
+      tmem_ld_x64(tmem_addr(tmem, 32 * q4, kColD1), x);
+      tc_fence_before();
+      mbar_arrive(&bar[bD1Empty]);
+      if (akk) {
+        // row r of A: beta_r Akk[r][i] for i < r, zero elsewhere
+        float* arow = Am + r * kLd;
+#pragma unroll
+        for (int i = 0; i < 64; i += 4) {
+          float a4[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) a4[j] = (i + j < r) ? br * __uint_as_float(x[i + j]) : 0.f;
+          *reinterpret_cast<float4*>(arow + i) = make_float4(a4[0], a4[1], a4[2], a4[3]);
         }
-        if (akk) {
-          // row r of A: beta_r Akk[r][i] for i < r, zero elsewhere
-          float* arow = Am + r * kLd;
+        sB[r] = br;
+      } else {
+        // Aqk row r (causal mask): bf16 operand tile of O^T += Delta^T Aqk^T
+        // (without scale: the state pass multiplies O by scale at the end);
+        // the tile of chunk c-2 must be done
+        if (c >= 2) wait_bar(&bar[bHiFree + (c & 1)], par((c >> 1) - 1), abort_flag, P.status);
+        uint8_t* aqkb = sm + Lay::AQKB + (c & 1) * 8192;
 #pragma unroll
-          for (int i = 0; i < 64; i += 4) {
-            float a4[4];
+        for (int i = 0; i < 64; i += 8) {
+          float f[8];
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-              a4[j] = (i + j < r) ? br * __uint_as_float(i + j < 32 ? xa[i + j] : xb[i + j - 32]) : 0.f;
-            *reinterpret_cast<float4*>(arow + i) = make_float4(a4[0], a4[1], a4[2], a4[3]);
-          }
-          sB[r] = br;
-        } else {
-          // Aqk row r (causal mask): bf16 operand tile of O^T += Delta^T Aqk^T
-          // (without scale: the state pass multiplies O by scale at the end);
-          // the tile of chunk c-2 must be done
-          if (c >= 2) wait_bar(&bar[bHiFree + (c & 1)], par((c >> 1) - 1), abort_flag, P.status);
-          uint8_t* aqkb = sm + Lay::AQKB + (c & 1) * 8192;
+          for (int j = 0; j < 8; ++j) f[j] = (i + j <= r) ? __uint_as_float(x[i + j]) : 0.f;
+          *reinterpret_cast<uint4*>(aqkb + sw128_offset(uint32_t(r), uint32_t(i), 64)) = pack8(f);
+        }
+        fence_proxy_async_smem();
+        // and the fp32 Aqk row (scaled, causal mask), 32 bytes a store when
+        // the output is 32-byte aligned
+        if (A.Aqk && r < L) {
+          float* arow = A.Aqk + (size_t(t0 + r) * P.Hv + hv) * 64;
 #pragma unroll
           for (int i = 0; i < 64; i += 8) {
             float f[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) f[j] = (i + j <= r) ? __uint_as_float(i + j < 32 ? xa[i + j] : xb[i + j - 32]) : 0.f;
-            *reinterpret_cast<uint4*>(aqkb + sw128_offset(uint32_t(r), uint32_t(i), 64)) = pack8(f);
+            for (int j = 0; j < 8; ++j) f[j] = (i + j <= r) ? P.scale * __uint_as_float(x[i + j]) : 0.f;
+            const float4 lo4 = make_float4(f[0], f[1], f[2], f[3]), hi4 = make_float4(f[4], f[5], f[6], f[7]);
+            if (A.aqk_v8) {
+              st_global_v8(arow + i, lo4, hi4);  // a whole 32-byte sector per thread
+            } else {
+              *reinterpret_cast<float4*>(arow + i) = lo4;
+              *reinterpret_cast<float4*>(arow + i + 4) = hi4;
+            }
           }
-          fence_proxy_async_smem();
         }
       }
       named_bar_sync(kNbIntra, 128);
-      // ---- X = (I + A)^-1 by 16 x 16 blocks.  Diagonal blocks: forward
-      // substitution, thread = (block d, column cc), on the threads that wrote A.
       if (akk) {
+        // ---- X = (I + A)^-1 by 16 x 16 blocks.  Diagonal blocks: forward
+        // substitution, thread = (block d, column cc), on the threads that
+        // wrote A; right-looking (once x[i] is final it leaves the rows below),
+        // so the dependent chain is one FMA a row
         const int d = (e - 64) >> 4, cc = e & 15, base = 16 * d;
-        float x[16];
+        const float* ab = Am + base * kLd + base;
+        float xc[16];
 #pragma unroll
-        for (int rr = 0; rr < 16; ++rr) {
-          float acc = 0.f;
+        for (int rr = 0; rr < 16; ++rr) xc[rr] = rr == cc ? 1.f : 0.f;
 #pragma unroll
-          for (int i = 0; i < rr; ++i) acc = fmaf(Am[(base + rr) * kLd + base + i], x[i], acc);
-          x[rr] = (rr == cc ? 1.f : 0.f) - acc;
-        }
+        for (int i = 0; i < 15; ++i)
+#pragma unroll
+          for (int rr = i + 1; rr < 16; ++rr) xc[rr] = fmaf(-ab[rr * kLd + i], xc[i], xc[rr]);
         uint8_t* b2 = sm + Lay::B2;
         const float bc = sB[base + cc];
 #pragma unroll
         for (int rr = 0; rr < 16; ++rr) {
-          Xm[(base + rr) * kLd + base + cc] = x[rr];
+          Xm[(base + rr) * kLd + base + cc] = xc[rr];
           *reinterpret_cast<__nv_bfloat16*>(b2 + sw128_offset(uint32_t(base + rr), uint32_t(base + cc), 64)) =
-              __float2bfloat16_rn(x[rr] * bc);
+              __float2bfloat16_rn(xc[rr] * bc);
         }
       }
       named_bar_sync(kNbIntra, 128);
@@ -652,54 +654,21 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         umma_commit(&bar[bD2Full]);
       }
       __syncwarp();
-      // ---- exports after MMA2: Akk_inv by whole rows from the scratch (8
-      // passes of 8 rows x 16 column quads, all 128 threads), then the lo area
-      // is free; then the Aqk warps read their rows of D1 again (releasing it)
-      // and write Aqk (scaled, causal mask), 32 bytes a store when the output
-      // is 32-byte aligned
+      // ---- Akk_inv = X (lower triangle), by whole rows from the scratch (8
+      // passes of 8 rows x 16 column quads), while MMA2 runs
       if (A.Akk_inv) {
 #pragma unroll 2
         for (int it = 0; it < 8; ++it) {
           const int row = 8 * it + (e >> 4), c4 = 4 * (e & 15);
-          if (row < L) {
-            const float4 xv = *reinterpret_cast<const float4*>(Xm + row * kLd + c4);
-            const float4 o4 = make_float4(c4 <= row ? xv.x : 0.f, c4 + 1 <= row ? xv.y : 0.f,
-                                          c4 + 2 <= row ? xv.z : 0.f, c4 + 3 <= row ? xv.w : 0.f);
-            *reinterpret_cast<float4*>(A.Akk_inv + (size_t(t0 + row) * P.Hv + hv) * 64 + c4) = o4;
-          }
+          const float4 xv = *reinterpret_cast<const float4*>(Xm + row * kLd + c4);
+          const float4 o4 = make_float4(c4 <= row ? xv.x : 0.f, c4 + 1 <= row ? xv.y : 0.f,
+                                        c4 + 2 <= row ? xv.z : 0.f, c4 + 3 <= row ? xv.w : 0.f);
+          if (row < L) *reinterpret_cast<float4*>(A.Akk_inv + (size_t(t0 + row) * P.Hv + hv) * 64 + c4) = o4;
         }
       }
-      mbar_arrive(&bar[bLoFree]);
-      if (!akk) {
-        float* arow = A.Aqk + (size_t(t0 + r) * P.Hv + hv) * 64;
-        const bool wr = A.Aqk && r < L;
-        uint32_t x[64];
-        tmem_ld_x64(tmem_addr(tmem, 32 * q4, kColD1), x);
-        tc_fence_before();
-        mbar_arrive(&bar[bD1Empty]);
-        if (wr) {
-#pragma unroll
-          for (int i = 0; i < 64; i += 8) {
-            float f[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) f[j] = (i + j <= r) ? P.scale * __uint_as_float(x[i + j]) : 0.f;
-            const float4 lo4 = make_float4(f[0], f[1], f[2], f[3]), hi4 = make_float4(f[4], f[5], f[6], f[7]);
-            if (A.aqk_v8) {
-              st_global_v8(arow + i, lo4, hi4);  // a whole 32-byte sector per thread
-            } else {
-              *reinterpret_cast<float4*>(arow + i) = lo4;
-              *reinterpret_cast<float4*>(arow + i + 4) = hi4;
-            }
-          }
-        }
-      }
-      // ---- MMA2 is done with the v tile: copy the next chunk's v
-      wait_bar(&bar[bD2Full], par(c), abort_flag, P.status);
-      if (leader && c + 1 < nch) load_v(c + 1);
     }
     if (leader) {
-      // after an abort: the last v copy and the last MMA2 must land before exit
-      mbar_wait(&bar[bVFull], par(nch - 1), kDrainNs);
+      // after an abort: the last MMA2 must land before exit
       umma_commit(&bar[bDrain + 1]);
       mbar_wait(&bar[bDrain + 1], 0, kDrainNs);
     }
@@ -708,155 +677,163 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     // =============================================================== state
     regs_dec<kRegsState>();
     const int q4 = warp & 3;
-    const int v = 32 * q4 + lane;  // value channel = TMEM lane
-    const bool vv = v < V;
+    const int v = 32 * q4 + lane;  // TMEM lane: value channel v (S^T, U^T, P^T, O^T), channel k of W^T
+    const bool vv = v < V, kk = v < K;
     const bool leader = warp == kWarpState0 && lane == 0;
-    uint8_t* st = sm + Lay::ST;
-    uint8_t* wd = sm + Lay::WD;
+    uint8_t* ust = sm + Lay::UST;
     const float* gam_base = reinterpret_cast<const float*>(sm + Lay::GAM);
     const uint32_t lane_base = tmem_addr(tmem, 32 * q4, 0);
-    // row v of the bf16 S^T tile, columns j .. j + 31
-    auto store_st = [&](int j, const uint32_t (&s)[32]) {
+    // In a token-major SWIZZLE_128B tile (64-channel atoms of 64 token rows x
+    // 128 B, what a TMA store of a (64, 1, 64) box reads), this thread's
+    // channel sits at byte swz[t % 8] of row t of its atom: the 16-byte chunk
+    // index is XOR-ed by (row % 8).
+    uint32_t swz[8];
 #pragma unroll
-      for (int i = 0; i < 32; i += 8) {
-        float f[8];
+    for (int r8 = 0; r8 < 8; ++r8) swz[r8] = ((uint32_t(((v & 63) >> 3) ^ r8)) << 4) | (uint32_t(v & 7) << 1);
+    // 32 token rows t0 .. t0 + 31 of one channel (values x) into such a tile
+    auto stage32 = [&](uint8_t* atom, int t0r, const uint32_t (&x)[32], float s) {
 #pragma unroll
-        for (int u = 0; u < 8; ++u) f[u] = __uint_as_float(s[i + u]);
-        *reinterpret_cast<uint4*>(st + sw128_offset(uint32_t(v), uint32_t(j + i), 128)) = pack8(f);
-      }
+      for (int j = 0; j < 32; ++j)
+        *reinterpret_cast<__nv_bfloat16*>(atom + (t0r + j) * 128 + swz[j & 7]) =
+            __float2bfloat16_rn(s * __uint_as_float(x[j]));
     };
-    // O of chunk cc (TMEM buffer cc % 2) to o, scaled
-    auto read_o = [&](int cc) {
-      const int t0 = bos + cc * kChunk, L = min(kChunk, len - cc * kChunk);
-      uint32_t o[32];
+    // the same 32 values straight to a token-major global tensor (row stride
+    // `stride` elements), rows past the chunk's end skipped
+    auto store32 = [&](__nv_bfloat16* dst, size_t stride, int rows, const uint32_t (&x)[32], float s) {
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        tmem_ld_x32(lane_base + kColO + 64 * (cc & 1) + 32 * h, o);
-        if (vv) {
-          __nv_bfloat16* dst = A.o + (size_t(t0 + 32 * h) * P.Hv + hv) * V + v;
-#pragma unroll
-          for (int t = 0; t < 32; ++t)
-            if (32 * h + t < L) dst[size_t(t) * P.Hv * V] = __float2bfloat16_rn(P.scale * __uint_as_float(o[t]));
-        }
-      }
+      for (int j = 0; j < 32; ++j)
+        if (j < rows) dst[size_t(j) * stride] = __float2bfloat16_rn(s * __uint_as_float(x[j]));
     };
-    // initial state into TMEM (fp32) and the bf16 A operand
+    // S^T (fp32, columns j .. j + 31) into TMEM and its bf16 copy (the A operand)
+    auto put_state = [&](int j, const uint32_t (&s)[32]) {
+      tmem_st_x32(lane_base + kColS + j, s);
+      uint32_t b[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) b[i] = pack_bf16x2(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1]));
+      tmem_st_x16(lane_base + kColSb + j / 2, b);
+    };
+    // initial state
 #pragma unroll 1
     for (int j = 0; j < K; j += 32) {
       uint32_t s[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) s[i] = __float_as_uint((A.h0 && vv) ? A.h0[(hrow + j + i) * V + v] : 0.f);
-      tmem_st_x32(lane_base + kColS + j, s);
-      store_st(j, s);
+      put_state(j, s);
     }
     tmem_st_wait();
-    fence_proxy_async_smem();
     tc_fence_before();
     named_bar_sync(kNbState, 128);
+    constexpr uint32_t id64 = idesc_bf16_f32(128, 64);
+    constexpr uint32_t idH = idesc_bf16_f32(128, K) | kIdescBMajorMN;
     for (int c = 0; c < nch; ++c) {
-      const int L = min(kChunk, len - c * kChunk);
-      const uint32_t hi_addr = smem_u32(sm + Lay::HI + (c & 1) * Lay::kHi);
-      const uint32_t ocol = kColO + 64 * (c & 1);
-      // W^T (TMEM lane = channel k) into the W tile, MN-major: row k holds its
-      // 64 tokens.  The tile's previous reader, the H MMA of chunk c-1, is done.
-      // MMA2 commits after the Aqk_b tile of chunk c was written (its issuer
-      // waits for the intra warps first), so D2 full also covers that tile.
+      const int t0 = bos + c * kChunk, L = min(kChunk, len - c * kChunk);
+      const bool full = L == kChunk;  // a TMA box of 64 token rows stays inside the sequence
+      uint8_t* hi = sm + Lay::HI + (c & 1) * Lay::kHi;
+      const uint32_t hi_addr = smem_u32(hi);
+      // ---- W^T (TMEM lane = channel k) into the W tile, token-major, in the
+      // Kg rows of this chunk's A1_hi (MMA2 was their last reader): atom a at
+      // hi + 16 KB a + 8 KB.  MMA2 commits after the Aqk_b tile of chunk c was
+      // written, so D2 full also covers that tile.
       wait_bar(&bar[bD2Full], par(c), abort_flag, P.status);
       tc_fence_after();
-      const int t0 = bos + c * kChunk;
+      if (leader && c + 1 < nch) {
+        // MMA2 is done with the v tile: the TMA copy of the next chunk's v
+        mbar_arrive_expect_tx(&bar[bVFull], uint32_t(V) * 64u * 2u);
+#pragma unroll
+        for (int a = 0; a < V / 64; ++a)
+          tma_load_3d(sm + Lay::VT + a * 8192, &maps.v_sw, a * 64, hv, t0 + kChunk, &bar[bVFull]);
+      }
+      const bool w_tma = A.W && A.w_tma && full;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint32_t w[32];
         tmem_ld_x32(lane_base + kColW + 32 * h, w);
-        if (v < K) {
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            float f[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(w[8 * j + i]);
-            *reinterpret_cast<uint4*>(wd + v * 128 + ((uint32_t(4 * h + j) ^ uint32_t(v & 7)) << 4)) = pack8(f);
-          }
+        if (kk) {
+          stage32(hi + (v >> 6) * 16384 + 8192, 32 * h, w, 1.f);
+          if (A.W && !w_tma)
+            store32(reinterpret_cast<__nv_bfloat16*>(A.W) + (size_t(t0 + 32 * h) * P.Hv + hv) * K + v,
+                    size_t(P.Hv) * K, L - 32 * h, w, 1.f);
         }
       }
       fence_proxy_async_smem();
       tc_fence_before();
+      if (leader) bulk_wait_read_all();  // the last chunk's o store has read the U tile
       named_bar_sync(kNbState, 128);
       if (leader) {
-        // P^T = S^T W^T (W tile MN-major: a K step of 16 channels is 2048 B), then
-        // O^T = S^T Qg^T (Qg rows 0-63 of A1_hi, K-major)
+        // P^T = S^T W^T into the W^T columns (read above), then O^T = S^T Qg^T;
+        // A = S^T from TMEM, B = the W tile / the Qg rows (K-major, atoms 16 KB
+        // apart); then the W tile's TMA store
         tc_fence_after();
-        constexpr uint32_t idP = idesc_bf16_f32(128, 64) | kIdescBMajorMN;
-        constexpr uint32_t id64 = idesc_bf16_f32(128, 64);
-        const uint64_t a_st = sdesc_kmajor_sw128(smem_u32(st));
-        const uint64_t b_w = sdesc_mnmajor_sw128(smem_u32(wd), 8192);
-        const uint64_t b_qg = sdesc_kmajor_sw128(hi_addr);
+        const uint64_t b_w = sdesc_kmajor_sw128(hi_addr + 8192), b_qg = sdesc_kmajor_sw128(hi_addr);
 #pragma unroll
-        for (int g = 0; g < K / 64; ++g) umma_k4(tmem + kColP, a_st + g * 1024, b_w + g * 512, idP, g > 0, 2, 128);
+        for (int g = 0; g < K / 64; ++g) umma_ts4(tmem + kColW, tmem + kColSb + 32 * g, b_w + g * 1024, id64, g > 0, 2);
         umma_commit(&bar[bPDone]);
 #pragma unroll
-        for (int g = 0; g < K / 64; ++g) umma_atom4(tmem + ocol, a_st + g * 1024, b_qg + g * 1024, id64, g > 0);
+        for (int g = 0; g < K / 64; ++g)
+          umma_ts4(tmem + kColO, tmem + kColSb + 32 * g, b_qg + g * 1024, id64, g > 0, 2);
+        if (w_tma) {
+#pragma unroll
+          for (int a = 0; a < K / 64; ++a) tma_store_3d(&maps.W, hi + a * 16384 + 8192, a * 64, hv, t0);
+          bulk_commit_group();
+        }
       }
       __syncwarp();
-      // exports while P runs: W of this chunk (thread = channel k), o of the last
-      if (A.W) {
-#pragma unroll 1
-        for (int h = 0; h < 2; ++h) {
-          uint32_t w[32];
-          tmem_ld_x32(lane_base + kColW + 32 * h, w);  // W^T again: D2 stays valid until this chunk's Delta
-          if (v < K) {
-            __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(A.W) + (size_t(t0 + 32 * h) * P.Hv + hv) * K + v;
-#pragma unroll
-            for (int t = 0; t < 32; ++t)
-              if (32 * h + t < L) dst[size_t(t) * P.Hv * K] = __float2bfloat16_rn(__uint_as_float(w[t]));
-          }
-        }
-      }
-      if (c >= 1) read_o(c - 1);
+      // ---- Delta^T row v = U^T - P^T (tokens past the chunk's end zero) into
+      // TMEM as bf16 pairs; U^T to its staging tile (or straight out)
       wait_bar(&bar[bPDone], par(c), abort_flag, P.status);
       tc_fence_after();
-      // Delta^T row v: U^T - P^T, tokens past the chunk's end zero (into the W
-      // tile's area: P, its only reader, is done)
+      const bool u_tma = A.U && A.u_tma && full;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        uint32_t pr[32], ur[32];
-        tmem_ld_x32(lane_base + kColP + 32 * h, pr);
+        uint32_t ur[32];
         tmem_ld_x32(lane_base + kColU + 32 * h, ur);
 #pragma unroll
-        for (int j = 0; j < 32; j += 8) {
-          float d[8];
+        for (int q = 0; q < 2; ++q) {
+          uint32_t pr[16], dw[8];
+          tmem_ld_x16(lane_base + kColW + 32 * h + 16 * q, pr);
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            d[i] = (vv && 32 * h + j + i < L) ? __uint_as_float(ur[j + i]) - __uint_as_float(pr[j + i]) : 0.f;
-          *reinterpret_cast<uint4*>(wd + v * 128 + ((uint32_t((32 * h + j) >> 3) ^ uint32_t(v & 7)) << 4)) = pack8(d);
+          for (int i = 0; i < 8; ++i) {
+            const int t = 32 * h + 16 * q + 2 * i;
+            const float d0 = (vv && t < L) ? __uint_as_float(ur[16 * q + 2 * i]) - __uint_as_float(pr[2 * i]) : 0.f;
+            const float d1 =
+                (vv && t + 1 < L) ? __uint_as_float(ur[16 * q + 2 * i + 1]) - __uint_as_float(pr[2 * i + 1]) : 0.f;
+            dw[i] = pack_bf16x2(d0, d1);
+          }
+          tmem_st_x8(lane_base + kColDt + 16 * h + 8 * q, dw);
         }
         if (A.U && vv) {
-          __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(A.U) + (size_t(t0 + 32 * h) * P.Hv + hv) * V + v;
-#pragma unroll
-          for (int t = 0; t < 32; ++t)
-            if (32 * h + t < L) dst[size_t(t) * P.Hv * V] = __float2bfloat16_rn(__uint_as_float(ur[t]));
+          if (u_tma)
+            stage32(ust + (v >> 6) * 8192, 32 * h, ur, 1.f);
+          else
+            store32(reinterpret_cast<__nv_bfloat16*>(A.U) + (size_t(t0 + 32 * h) * P.Hv + hv) * V + v,
+                    size_t(P.Hv) * V, L - 32 * h, ur, 1.f);
         }
       }
+      tmem_st_wait();
+      fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&bar[bD2Empty]);
-      fence_proxy_async_smem();
       named_bar_sync(kNbState, 128);
       if (leader) {
         // S^T += Delta^T Kd (Kd token rows of B1_hi as an MN-major B: 64-channel
-        // blocks 8 KB apart, a K step of 16 tokens 2048 B), O^T += Delta^T Aqk^T
+        // blocks 8 KB apart, a K step of 16 tokens 2048 B), O^T += Delta^T Aqk^T;
+        // A = Delta^T from TMEM.  Then U's TMA store.
         tc_fence_after();
-        constexpr uint32_t idH = idesc_bf16_f32(128, K) | kIdescBMajorMN;
-        constexpr uint32_t id64 = idesc_bf16_f32(128, 64);
-        const uint64_t a_d = sdesc_kmajor_sw128(smem_u32(wd));
         const uint64_t b_kd = sdesc_mnmajor_sw128(hi_addr + Lay::kA1, 8192);
         const uint64_t b_aqk = sdesc_kmajor_sw128(smem_u32(sm + Lay::AQKB + (c & 1) * 8192));
-        umma_k4(tmem + kColS, a_d, b_kd, idH, 1, 2, 2048 / 16);
-        umma_atom4(tmem + ocol, a_d, b_aqk, id64, 1);
+        umma_ts4(tmem + kColS, tmem + kColDt, b_kd, idH, 1, 2048 / 16);
+        umma_ts4(tmem + kColO, tmem + kColDt, b_aqk, id64, 1, 2);
         umma_commit(&bar[bHODone]);
+        if (u_tma) {
+#pragma unroll
+          for (int a = 0; a < V / 64; ++a) tma_store_3d(&maps.U, ust + a * 8192, a * 64, hv, t0);
+          bulk_commit_group();
+        }
       }
       __syncwarp();
       wait_bar(&bar[bHODone], par(c), abort_flag, P.status);
       tc_fence_after();
-      // S <- gamma * (S + Kd^T Delta), in TMEM and as the bf16 A operand
+      // ---- S <- gamma * (S + Kd^T Delta), in TMEM (fp32 and the bf16 A operand)
       const float* gm = gam_base + (c & 1) * K;
 #pragma unroll 1
       for (int j = 0; j < K; j += 32) {
@@ -870,17 +847,39 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
           s[i + 2] = __float_as_uint(__uint_as_float(s[i + 2]) * g4.z);
           s[i + 3] = __float_as_uint(__uint_as_float(s[i + 3]) * g4.w);
         }
-        tmem_st_x32(lane_base + kColS + j, s);
-        store_st(j, s);
+        put_state(j, s);
+      }
+      // ---- the W and U stores have read their tiles: the hi buffer (with its
+      // gamma and Aqk tile) goes back to the prep and intra warps
+      if (leader) bulk_wait_read_all();
+      named_bar_sync(kNbState, 128);
+      mbar_arrive(&bar[bHiFree + (c & 1)]);
+      // ---- o = scale O^T, staged token-major in the U tile (its store is done)
+      const bool o_tma = A.o_tma && full;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t o[32];
+        tmem_ld_x32(lane_base + kColO + 32 * h, o);
+        if (vv) {
+          if (o_tma)
+            stage32(ust + (v >> 6) * 8192, 32 * h, o, P.scale);
+          else
+            store32(A.o + (size_t(t0 + 32 * h) * P.Hv + hv) * V + v, size_t(P.Hv) * V, L - 32 * h, o, P.scale);
+        }
       }
       tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&bar[bHiFree + (c & 1)]);
-      // (the next chunk's barrier after its W tile also orders these S^T writes
-      // before its P MMA)
+      named_bar_sync(kNbState, 128);
+      if (leader && o_tma) {
+#pragma unroll
+        for (int a = 0; a < V / 64; ++a) tma_store_3d(&maps.o, ust + a * 8192, a * 64, hv, t0);
+        bulk_commit_group();
+      }
+      __syncwarp();
+      // (the next chunk's barrier after its W tile also orders these S^T
+      // writes before its P MMA)
     }
-    read_o(nch - 1);
     if (A.hT) {
 #pragma unroll 1
       for (int j = 0; j < K; j += 32) {
@@ -892,6 +891,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       }
     }
     if (leader) {
+      // after an abort: the last v copy (issued here or by the intra leader) lands before exit
+      mbar_wait(&bar[bVFull], par(nch - 1), kDrainNs);
+      bulk_wait_all();
       umma_commit(&bar[bDrain + 2]);
       mbar_wait(&bar[bDrain + 2], 0, kDrainNs);
     }
@@ -905,7 +907,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
 }
 
 template <int K, int V, bool kQG>
-cudaError_t launch_fused_t(const Problem& P, const FusedArgs& A, const IntraMaps& maps, int dev, cudaStream_t s) {
+cudaError_t launch_fused_t(const Problem& P, const FusedArgs& A, const FusedMaps& maps, int dev, cudaStream_t s) {
   constexpr uint32_t smem = FusedLayout<K, V>::bytes;
   cudaError_t e = set_smem_once<fused_kernel<K, V, kQG>>(smem, dev);
   if (e != cudaSuccess) return e;
@@ -917,7 +919,7 @@ cudaError_t launch_fused_t(const Problem& P, const FusedArgs& A, const IntraMaps
 
 }  // namespace
 
-cudaError_t launch_fused(const Problem& P, const FusedArgs& A, const IntraMaps& maps, int dev, cudaStream_t s) {
+cudaError_t launch_fused(const Problem& P, const FusedArgs& A, const FusedMaps& maps, int dev, cudaStream_t s) {
   // The optional QG export has its own instantiations, so that the usual
   // prep loop carries none of its code.
   const bool qg = A.QG != nullptr;

@@ -137,6 +137,13 @@ struct IntraMaps {
   CUtensorMap v_sw;        // v, SWIZZLE_128B boxes of (64, 1, 64): the W/U MMA's A operand, MN-major
 };
 
+// The fused forward's maps: the intra maps' inputs plus the outputs written
+// by TMA stores from token-major SWIZZLE_128B tiles, boxes of (64, 1, 64).
+struct FusedMaps {
+  CUtensorMap q, k, v, g, v_sw;
+  CUtensorMap o, W, U;
+};
+
 struct StateMaps {
   CUtensorMap W, Qs, Aqk_b, U, Kl;
 };
@@ -157,6 +164,7 @@ struct FusedArgs {
   float* G;                 // fp32 [BT, Hv, K] or null
   void* QG;                 // bf16 [BT, Hv, K] or null
   int aqk_v8;               // Aqk is 32-byte aligned: its rows are written with 32-byte stores
+  int o_tma, w_tma, u_tma;  // o / W / U have a store map: whole chunks leave by TMA stores
 };
 
 cudaError_t launch_chunk_index(const int32_t* cu, int N, int T, int chunk, int32_t* idx, int32_t* off,
@@ -169,6 +177,6 @@ cudaError_t launch_intra(const Problem& P, const IntraInputs& in, const IntraOut
                          int dev, int sms, cudaStream_t s);
 cudaError_t launch_state(const Problem& P, const StateMaps& maps, const float* gamma, const float* h0,
                          void* o, float* hT, int dev, cudaStream_t s);
-cudaError_t launch_fused(const Problem& P, const FusedArgs& A, const IntraMaps& maps, int dev, cudaStream_t s);
+cudaError_t launch_fused(const Problem& P, const FusedArgs& A, const FusedMaps& maps, int dev, cudaStream_t s);
 
 }  // namespace kda

@@ -481,10 +481,12 @@ def main():
             "vs_baseline": (value / (B * T / (page * 1e-3))) if page else None,
             "dtype": "bf16", "data": "synthetic", "config": config,
             "kernels_ms": kern, "roofline": roof, "path_roofline": path, "cpu_baseline": cpu, "e2e": e2e,
-            # per step: the fused kernel, or intra + state; varlen adds the
-            # sequence-order kernel (and, on the two-pass path, the chunk table)
-            "gpu_launches": args.steps * ((1 if fused else 2) + (0 if host["cu_seqlens"] is None else
-                                                                 (1 if fused else 2))),
+            # per step: the fused kernel, or intra + state, then the exact
+            # path's check of the chain flags (its CTAs return at once unless a
+            # chunk passed the gate range); varlen adds the sequence-order
+            # kernel (and, on the two-pass path, the chunk table)
+            "gpu_launches": args.steps * ((1 if fused else 2) + 1 + (0 if host["cu_seqlens"] is None else
+                                                                     (1 if fused else 2))),
             "path": "fused" if fused else "two_pass",
             "clocks": clocks}
     print(json.dumps(line))

@@ -47,7 +47,8 @@ bool map_tokens(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int es
 }
 
 struct Layout {
-  size_t status = 0, nc = 4, idx = 0, off = 0, order = 0, Qs = 0, Aqk_b = 0, Kl = 0, gamma = 0, W = 0, U = 0, total = 0;
+  size_t status = 0, nc = 4, flags = 0, flags_bytes = 0, idx = 0, off = 0, order = 0, Qs = 0, Aqk_b = 0, Kl = 0,
+         gamma = 0, W = 0, U = 0, total = 0;
 };
 
 struct Shape {
@@ -114,6 +115,9 @@ Layout make_layout(const Shape& s, const KdaArgs* a, Mode mode) {
     p = align_up(p + bytes);
     return at;
   };
+  // per-chain flags of the exact path, cleared with the header by one memset
+  L.flags_bytes = size_t(s.N) * s.Hv * 4;
+  L.flags = take(L.flags_bytes);
   if (s.varlen && mode != Mode::kFused && !a->chunk_indices) {
     L.idx = take(size_t(s.nc_max > 0 ? s.nc_max : 1) * 2 * 4);
     L.off = take(size_t(s.N + 1) * 4);
@@ -201,6 +205,7 @@ Problem make_problem(const Shape& s, const KdaArgs* a, uint8_t* ws, const Layout
   P.scale = a->scale;
   P.cu = a->cu_seqlens;
   P.status = reinterpret_cast<int32_t*>(ws + L.status);
+  P.flags = reinterpret_cast<int32_t*>(ws + L.flags);
   if (s.varlen) {
     if (a->chunk_indices) {
       P.chunk_idx = a->chunk_indices;
@@ -234,7 +239,7 @@ int prologue(const KdaArgs* a, void* workspace, size_t ws_bytes, cudaStream_t st
   if (rc) return rc;
   if (!encode_fn()) return KDA_ERR_LAUNCH;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  if (cudaMemsetAsync(ws, 0, 8, st) != cudaSuccess) return KDA_ERR_LAUNCH;
+  if (cudaMemsetAsync(ws, 0, L->flags + L->flags_bytes, st) != cudaSuccess) return KDA_ERR_LAUNCH;
   if (s->varlen && s->N > 0) {
     int32_t* status = reinterpret_cast<int32_t*>(ws + L->status);
     if (a->chunk_indices) {
@@ -283,6 +288,29 @@ int empty_forward(const Shape& s, const KdaArgs* a, cudaStream_t st) {
   return e == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
 }
 
+// The exact path: recomputes the chains the tensor-core kernels marked (a
+// chunk past the gate range); a chain left unmarked costs one flag read.
+int run_exact(const KdaArgs* a, const Problem& P, const DeviceInfo& d, bool state, cudaStream_t st) {
+  ExactArgs x{};
+  x.q = a->q;
+  x.k = a->k;
+  x.v = a->v;
+  x.g = a->g;
+  x.beta = a->beta;
+  x.h0 = a->initial_state;
+  x.o = reinterpret_cast<__nv_bfloat16*>(a->o);
+  x.hT = a->final_state;
+  x.Aqk = a->Aqk;
+  x.Akk_inv = a->Akk_inv;
+  x.W = a->W;
+  x.U = a->U;
+  x.G = a->G;
+  x.QG = a->QG;
+  x.flags = P.flags;
+  x.state = state ? 1 : 0;
+  return launch_exact(P, x, d.dev, st) == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
+}
+
 int two_pass_forward(const Shape& s, const KdaArgs* a, uint8_t* ws, const Layout& L, const DeviceInfo& d,
                      cudaEvent_t const* ev, cudaStream_t st) {
   const Problem P = make_problem(s, a, ws, L);
@@ -312,7 +340,7 @@ int two_pass_forward(const Shape& s, const KdaArgs* a, uint8_t* ws, const Layout
   if (launch_state(P, m, out.gamma, a->initial_state, a->o, a->final_state, d.dev, st) != cudaSuccess)
     return KDA_ERR_LAUNCH;
   if (ev && cudaEventRecord(ev[2], st) != cudaSuccess) return KDA_ERR_LAUNCH;
-  return KDA_OK;
+  return run_exact(a, P, d, true, st);
 }
 
 int fused_forward(const Shape& s, const KdaArgs* a, uint8_t* ws, const Layout& L, const DeviceInfo& d,
@@ -351,7 +379,7 @@ int fused_forward(const Shape& s, const KdaArgs* a, uint8_t* ws, const Layout& L
   if (launch_fused(P, f, m, d.dev, st) != cudaSuccess) return KDA_ERR_LAUNCH;
   if (ev && (cudaEventRecord(ev[1], st) != cudaSuccess || cudaEventRecord(ev[2], st) != cudaSuccess))
     return KDA_ERR_LAUNCH;
-  return KDA_OK;
+  return run_exact(a, P, d, true, st);
 }
 
 }  // namespace
@@ -403,7 +431,8 @@ extern "C" int kda_fwd_intra(const KdaArgs* a, void* workspace, size_t ws_bytes,
   out.U = a->U;
   out.G = a->G;
   out.QG = a->QG;
-  return run_intra(s, a, P, out, d, st);
+  rc = run_intra(s, a, P, out, d, st);
+  return rc ? rc : run_exact(a, P, d, false, st);
 }
 
 extern "C" int kda_prepare_chunk_indices(const int32_t* cu_seqlens, int32_t N, int32_t T, int32_t chunk,
@@ -471,7 +500,7 @@ extern "C" const char* kda_status_string(int status) {
     case KDA_ERR_BAD_SEQLENS: return "cu_seqlens must start at 0, be non-decreasing and end at T";
     case KDA_ERR_TIMEOUT: return "a bounded wait inside a kernel ran out";
     case KDA_ERR_GATE_RANGE:
-      return "a chunk's cumulative log-gate fell below -KDA_MAX_CHUNK_LOG_DECAY on some channel";
+      return "reserved (chains past the gate range are recomputed by the exact path)";
     case KDA_ERR_BAD_CHUNK_TABLE: return "the supplied chunk_indices / chunk_offsets do not match cu_seqlens";
     default: return "unknown status";
   }

@@ -379,9 +379,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       }
       // e^{G_r - G_i} is formed as the product of q e^{G_r} and k e^{-G_i}: both
       // stay normal fp32 numbers only while the chunk's log-decay on every
-      // channel is at most KDA_MAX_CHUNK_LOG_DECAY
+      // channel is at most KDA_MAX_CHUNK_LOG_DECAY.  Past it the chain is
+      // marked, and the exact path recomputes it after this kernel.
       if (kact && quarter == 0 && fminf(glast.x, glast.y) < -KDA_MAX_CHUNK_LOG_DECAY)
-        set_status(P.status, KDA_ERR_GATE_RANGE);
+        P.flags[size_t(n) * P.Hv + hv] = 1;
       // gated operands, all in registers before the waits: hi halves to the hi
       // tiles, lo halves to the lo area
       uint32_t qgh[kRows], kgh[kRows], kdh[kRows], qgl[kRows], kgl[kRows], kdl[kRows];

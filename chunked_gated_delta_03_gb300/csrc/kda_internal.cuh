@@ -32,6 +32,7 @@ struct Problem {
   const int32_t* nc_dev;     // varlen: number of chunks
   const int32_t* seq_order;  // varlen state pass: sequences by chunk count, most first
   int32_t* status;           // device status word
+  int32_t* flags;            // [N * Hv]: 1 marks a chain with a chunk past the tensor-core paths' gate range
 };
 
 // One chunk: flat token row t0 (into the [B*T] token axis), L valid rows,
@@ -167,6 +168,26 @@ struct FusedArgs {
   int o_tma, w_tma, u_tma;  // o / W / U have a store map: whole chunks leave by TMA stores
 };
 
+// Pointers of the exact path for strong gates (recomputes the flagged chains).
+struct ExactArgs {
+  const void* q;        // bf16 [BT, Hq, K]
+  const void* k;        // bf16 [BT, Hq, K]
+  const void* v;        // bf16 [BT, Hv, V]
+  const float* g;       // fp32 [BT, Hv, K]
+  const void* beta;     // bf16 or fp32 [BT, Hv]
+  const float* h0;      // fp32 [N, Hv, K, V] or null (zeros)
+  __nv_bfloat16* o;     // bf16 [BT, Hv, V] (forward only)
+  float* hT;            // fp32 [N, Hv, K, V] or null
+  float* Aqk;           // fp32 [BT, Hv, 64] or null
+  float* Akk_inv;       // fp32 [BT, Hv, 64] or null
+  void* W;              // bf16 [BT, Hv, K] or null
+  void* U;              // bf16 [BT, Hv, V] or null
+  float* G;             // fp32 [BT, Hv, K] or null
+  void* QG;             // bf16 [BT, Hv, K] or null
+  const int32_t* flags; // [N * Hv]
+  int state;            // 1: the forward (o, final state); 0: the intra primitive's outputs only
+};
+
 cudaError_t launch_chunk_index(const int32_t* cu, int N, int T, int chunk, int32_t* idx, int32_t* off,
                                int32_t* nc, int32_t* status, cudaStream_t s);
 cudaError_t launch_check_table(const int32_t* cu, int N, int T, int chunk, const int32_t* idx, const int32_t* off,
@@ -178,5 +199,6 @@ cudaError_t launch_intra(const Problem& P, const IntraInputs& in, const IntraOut
 cudaError_t launch_state(const Problem& P, const StateMaps& maps, const float* gamma, const float* h0,
                          void* o, float* hT, int dev, cudaStream_t s);
 cudaError_t launch_fused(const Problem& P, const FusedArgs& A, const FusedMaps& maps, int dev, cudaStream_t s);
+cudaError_t launch_exact(const Problem& P, const ExactArgs& A, int dev, cudaStream_t s);
 
 }  // namespace kda

@@ -11,7 +11,7 @@
 //        straight from global memory (coalesced, all in flight together);
 //        inclusive cumsum G of g down the rows (the quarters exchange partial
 //        sums); a chunk whose log-decay on some channel passes
-//        KDA_MAX_CHUNK_LOG_DECAY sets KDA_ERR_GATE_RANGE; gated operands
+//        KDA_MAX_CHUNK_LOG_DECAY marks its chain for the exact path; gated operands
 //        Qg = q*e^G, Kg = k*e^G, Kd = k*e^{-G}, split into bf16 hi + lo and
 //        written into K-major SWIZZLE_128B tiles A1 = [Qg; Kg] (128 x K, the
 //        Kg rows first for odd items), B1 = Kd (64 x K); the state-pass
@@ -312,9 +312,10 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
       }
       // The decay factors e^{G_r - G_i} are formed as products of q e^{G} and
       // k e^{-G}; both stay normal fp32 numbers only while the chunk's total
-      // log-decay on the channel is at most KDA_MAX_CHUNK_LOG_DECAY.
+      // log-decay on the channel is at most KDA_MAX_CHUNK_LOG_DECAY.  Past it
+      // the chain is marked, and the exact path recomputes it afterwards.
       if (kact && quarter == 0 && fminf(glast.x, glast.y) < -KDA_MAX_CHUNK_LOG_DECAY)
-        set_status(P.status, KDA_ERR_GATE_RANGE);
+        P.flags[size_t(ci.n) * P.Hv + hv] = 1;
       const float2 gam = make_float2(__expf(glast.x), __expf(glast.y));
       const size_t head_row = size_t(gc) * P.Hv + hv;
       if (kact && quarter == 0 && out.gamma) *reinterpret_cast<float2*>(out.gamma + head_row * K + c0) = gam;

@@ -65,13 +65,16 @@ extern "C" {
 
 typedef struct CUstream_st* kda_stream_t; /* a cudaStream_t; NULL = legacy default stream */
 
-/* Gate range.  The intra-chunk kernel forms each decay factor e^{G_r - G_i}
+/* Gate range.  The tensor-core kernels form each decay factor e^{G_r - G_i}
  * (G the in-chunk cumulative log-gate) as the product of the operands
- * q e^{G_r} and k e^{-G_i} on the tensor cores.  Both stay normal fp32 numbers
- * while a chunk's total log-decay on every channel, -G at its last row, is at
- * most this bound; a call whose input passes it sets the device status
- * KDA_ERR_GATE_RANGE (read with kda_get_device_status) and its outputs are
- * not valid.  Gates of the form -softplus(x)/16 decay a few units per chunk. */
+ * q e^{G_r} and k e^{-G_i}.  Both stay normal fp32 numbers while a chunk's
+ * total log-decay on every channel, -G at its last row, is at most this
+ * bound.  A (sequence, value head) chain with a chunk past it is marked by
+ * those kernels and recomputed, in the same call, by an exact FP32 path that
+ * takes every decay factor as one exponential of a non-positive exponent
+ * (slower: it runs on CUDA cores, one CTA per marked chain), so any gate
+ * gives valid outputs.  Gates of the form -softplus(x)/16 decay a few units
+ * per chunk and never take that path. */
 #define KDA_MAX_CHUNK_LOG_DECAY 60.0f
 
 enum kda_status {
@@ -84,7 +87,7 @@ enum kda_status {
   KDA_ERR_WORKSPACE = -6,    /* workspace smaller than kda_workspace_size() */
   KDA_ERR_BAD_SEQLENS = -16, /* (device) cu_seqlens not 0..T and non-decreasing */
   KDA_ERR_TIMEOUT = -17,     /* (device) a bounded wait inside a kernel ran out */
-  KDA_ERR_GATE_RANGE = -18,  /* (device) a chunk's cumulative log-gate fell below -KDA_MAX_CHUNK_LOG_DECAY */
+  KDA_ERR_GATE_RANGE = -18,  /* reserved: no call reports it (chains past the gate range take the exact path) */
   KDA_ERR_BAD_CHUNK_TABLE = -19 /* (device) a caller-supplied chunk table does not match cu_seqlens */
 };
 

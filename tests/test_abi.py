@@ -108,20 +108,24 @@ def test_two_pass_workspace_accounts_for_missing_w_u(lib):
     assert _lib.kda_workspace_size(without) - _lib.kda_workspace_size(with_wu) >= 2 * 128 * 2 * 64 * 2
 
 
-def test_fused_workspace_is_the_header_and_the_sequence_order(lib):
+def test_fused_workspace_is_the_header_flags_and_the_sequence_order(lib):
     # the fused path keeps every state-pass operand on chip: the workspace holds
-    # the 256-byte status header, plus the longest-first sequence order (one
-    # int32 per sequence, rounded up to 256 bytes) in varlen mode
-    assert _lib.kda_workspace_size(_args()) == 256
-    assert _lib.kda_workspace_size(_args(path=_lib.KDA_PATH_FUSED, T=1 << 20, Hv=64, Hq=64)) == 256
-    # varlen: the fused forward needs 256 + 512 bytes; kda_workspace_size also
-    # covers kda_fwd_intra on the same arguments, whose chunk table takes
-    # (T/64 + N) pairs (1024 bytes) and N + 1 offsets (512)
+    # the 256-byte status header, the per-chain flags of the exact path (one
+    # int32 per (sequence, value head), rounded up to 256 bytes) and, in varlen
+    # mode, the longest-first sequence order (one int32 per sequence, rounded up)
+    up = lambda n: (n + 255) // 256 * 256
+    assert _lib.kda_workspace_size(_args()) == 256 + up(1 * 2 * 4)
+    assert _lib.kda_workspace_size(_args(path=_lib.KDA_PATH_FUSED, T=1 << 20, Hv=64, Hq=64)) == 256 + up(64 * 4)
+    # varlen, N = 100: the fused forward needs header + flags + order;
+    # kda_workspace_size also covers kda_fwd_intra on the same arguments, whose
+    # chunk table takes (T/64 + N) pairs and N + 1 offsets
     varlen = _args(cu_seqlens=1 << 20, N=100)
-    assert _lib.kda_workspace_size(varlen) == 256 + 1024 + 512
-    assert _lib.kda_chunk_fwd(varlen, 1 << 24, 256 + 512 - 1, 0) == _lib.KDA_ERR_WORKSPACE
-    intra = _args(cu_seqlens=1 << 20, N=100, Aqk=1 << 20, Akk_inv=1 << 20, W=1 << 20, U=1 << 20)
-    assert _lib.kda_fwd_intra(intra, 1 << 24, 256 + 1024 + 512 - 1, 0) == _lib.KDA_ERR_WORKSPACE
+    fused = 256 + up(100 * 2 * 4) + up(100 * 4)
+    intra = 256 + up(100 * 2 * 4) + up((128 // 64 + 100) * 2 * 4) + up(101 * 4)
+    assert _lib.kda_workspace_size(varlen) == max(fused, intra)
+    assert _lib.kda_chunk_fwd(varlen, 1 << 24, fused - 1, 0) == _lib.KDA_ERR_WORKSPACE
+    iargs = _args(cu_seqlens=1 << 20, N=100, Aqk=1 << 20, Akk_inv=1 << 20, W=1 << 20, U=1 << 20)
+    assert _lib.kda_fwd_intra(iargs, 1 << 24, intra - 1, 0) == _lib.KDA_ERR_WORKSPACE
 
 
 def test_workspace_size_ignores_optional_exports_and_precision(lib):

@@ -321,23 +321,70 @@ def test_strong_gates_within_range_match_oracle(path):
 
 
 @pytest.mark.parametrize("path", PATHS)
-def test_gates_past_the_range_set_device_status(path):
-    inp = _cuda(make_inputs(WORKLOADS["tiny"], seed=44, T=128))
-    inp["g"][:, 64:, 1, 5] = -1.0  # the second chunk decays by 64 on one channel of head 1
-    a, (B, T, Hq, Hv, K, V, N) = ops.make_args(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
-                                               inp["scale"], None, None)
+@pytest.mark.parametrize("decay", [64.0, 200.0])
+def test_gates_past_the_range_take_the_exact_path(path, decay):
+    # Every other channel of value head 1 decays by `decay` over each full
+    # chunk, past the range in which the tensor-core kernels' factorised decay
+    # operands k e^{-G} stay finite: those kernels mark the chain and the
+    # exact path recomputes it, while head 0 stays on the fast path.  The
+    # oracle forms e^{G_r - G_i} directly in FP64.
+    inp = make_inputs(WORKLOADS["tiny"], seed=44, T=200, K=128, V=128, initial_state=True)
+    g = inp["g"].clone()
+    g[:, :, 1, ::2] = -decay / 64
+    inp["g"] = g
+    want = _oracle(inp)
+    cin = _cuda(inp)
+    a, (B, T, Hq, Hv, K, V, N) = ops.make_args(cin["q"], cin["k"], cin["v"], cin["g"], cin["beta"],
+                                               cin["scale"], cin["initial_state"], None)
     a.path = ops._PATHS[path]
-    o = torch.zeros(B, T, Hv, V, dtype=torch.bfloat16, device="cuda")
-    a.o = o.data_ptr()
+    o = torch.full((B, T, Hv, V), float("nan"), dtype=torch.bfloat16, device="cuda")
+    fin = torch.full((N, Hv, K, V), float("nan"), dtype=torch.float32, device="cuda")
+    im = {"Aqk": torch.full((B, T, Hv, 64), float("nan"), dtype=torch.float32, device="cuda"),
+          "Akk_inv": torch.full((B, T, Hv, 64), float("nan"), dtype=torch.float32, device="cuda"),
+          "W": torch.full((B, T, Hv, K), float("nan"), dtype=torch.bfloat16, device="cuda"),
+          "U": torch.full((B, T, Hv, V), float("nan"), dtype=torch.bfloat16, device="cuda"),
+          "G": torch.full((B, T, Hv, K), float("nan"), dtype=torch.float32, device="cuda"),
+          "QG": torch.full((B, T, Hv, K), float("nan"), dtype=torch.bfloat16, device="cuda")}
+    a.o, a.final_state = o.data_ptr(), fin.data_ptr()
+    for key, t in im.items():
+        setattr(a, key, t.data_ptr())
     n = _lib.kda_workspace_size(a)
     ws = torch.empty(n, dtype=torch.uint8, device="cuda")
-    stream = torch.cuda.current_stream().cuda_stream
-    assert _lib.kda_chunk_fwd(a, ws.data_ptr(), n, stream) == _lib.KDA_OK
-    assert ops.device_status(ws) == _lib.KDA_ERR_GATE_RANGE
-    # back inside the range, a call on the same workspace clears the status
-    inp["g"][:, 64:, 1, 5] = -0.5
-    assert _lib.kda_chunk_fwd(a, ws.data_ptr(), n, stream) == _lib.KDA_OK
+    assert _lib.kda_chunk_fwd(a, ws.data_ptr(), n, torch.cuda.current_stream().cuda_stream) == _lib.KDA_OK
     assert ops.device_status(ws) == _lib.KDA_OK
+    _compare(inp, (o, fin, im), want, inter=True)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_strong_gates_in_one_packed_sequence(path):
+    # only the chain of the second sequence and head 0 passes the range (a
+    # decay of 96 per full chunk on eight channels); every other chain keeps
+    # the fast path, tails and an empty sequence included
+    inp = make_inputs(WORKLOADS["tiny"], seed=45, lengths=(70, 130, 0, 5, 64), Hq=2, Hv=2, K=64, V=64,
+                      initial_state=True, beta_dtype="bf16")
+    g = inp["g"].clone()
+    g[:, 70:200, 0, :8] = -1.5
+    inp["g"] = g
+    want = _oracle(inp)
+    out = _ours(_cuda(inp), inter=True, G=True, QG=True, path=path)
+    _compare(inp, out, want, inter=True)
+
+
+def test_intra_primitive_with_strong_gates():
+    inp = make_inputs(WORKLOADS["tiny"], seed=46, T=150, K=128, V=64)
+    g = inp["g"].clone()
+    g[:, :, 0, 3] = -2.0  # 128 per full chunk on one channel of head 0
+    inp["g"] = g
+    want = _oracle(inp)
+    cin = _cuda(inp)
+    intra = ops.chunk_kda_fwd_intra(cin["q"], cin["k"], cin["v"], cin["g"], cin["beta"], cin["scale"], None,
+                                    return_G=True, return_QG=True)
+    _check("Akk_inv", _np(intra["Akk_inv"]), want["Akk_inv"], **TOL_FP32)
+    _check("Aqk", _np(intra["Aqk"]), want["Aqk"], **TOL_FP32)
+    _check("W", _np(intra["W"]), want["W"], **TOL_WU)
+    _check("U", _np(intra["U"]), want["U"], **TOL_WU)
+    _check("G", _np(intra["G"]), want["G"], **TOL_G)
+    _check("QG", _np(intra["QG"]), want["QG"], **TOL_QG)
 
 
 @pytest.mark.parametrize("path", PATHS)

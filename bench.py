@@ -244,6 +244,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--path", choices=["auto", "fused", "two_pass"], default="auto")
+    ap.add_argument("--cp-chunks", type=int, default=0,
+                    help="intra-card context parallelism: segments of this many chunks (0: off)")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", "0"))
@@ -313,6 +315,7 @@ def main():
     a, _ = ops.make_args(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], dev["scale"],
                          dev["initial_state"], dev["cu_seqlens"])
     a.path = ops._PATHS[args.path]
+    a.cp_chunks = args.cp_chunks
     fused = args.path == "fused" or (args.path == "auto" and not a.intra_tf32)
     o = torch.empty(B, T, Hv, V, dtype=torch.bfloat16, device="cuda")
     fin = torch.empty(N, Hv, K, V, dtype=torch.float32, device="cuda")
@@ -388,6 +391,7 @@ def main():
             sa, _ = ops.make_args(din["q"], din["k"], din["v"], din["g"], din["beta"], dev["scale"],
                                   din.get("initial_state"), dev["cu_seqlens"])
             sa.path = a.path
+            sa.cp_chunks = a.cp_chunks
             sa.o, sa.final_state = dout["o"].data_ptr(), dout["final_state"].data_ptr()
             for name in ("Aqk", "Akk_inv", "W", "U"):
                 if name in dout:
@@ -485,8 +489,13 @@ def main():
             # path's check of the chain flags (its CTAs return at once unless a
             # chunk passed the gate range); varlen adds the sequence-order
             # kernel (and, on the two-pass path, the chunk table)
-            "gpu_launches": args.steps * ((1 if fused else 2) + 1 + (0 if host["cu_seqlens"] is None else
-                                                                     (1 if fused else 2))),
+            # (with --cp-chunks: the segment table, three passes of the fused
+            # kernel over the segments as packed sequences, each with its
+            # sequence order and flag check, the identity start states and
+            # the scan)
+            "gpu_launches": args.steps * (
+                (1 + 3 * 3 + 1 + 1) if (args.cp_chunks and -(-T // 64) > args.cp_chunks) else
+                ((1 if fused else 2) + 1 + (0 if host["cu_seqlens"] is None else (1 if fused else 2)))),
             "path": "fused" if fused else "two_pass",
             "clocks": clocks}
     print(json.dumps(line))

@@ -68,6 +68,7 @@ class KdaArgs(ctypes.Structure):
         ("path", ctypes.c_int32),
         ("chunk_indices", ctypes.c_void_p),
         ("chunk_offsets", ctypes.c_void_p),
+        ("cp_chunks", ctypes.c_int32),
     ]
 
 

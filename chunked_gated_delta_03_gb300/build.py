@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 LIB_DIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIB_DIR, "libkda.so")
 SOURCES = ["kda_api.cu", "kda_index.cu", "kda_intra.cu", "kda_state.cu", "kda_fused.cu", "kda_exact.cu",
-           "kda_static.cu"]
+           "kda_cp.cu", "kda_static.cu"]
 HEADERS = [os.path.join(CSRC, h) for h in ("kda_internal.cuh", "kda_ptx.cuh")] + [
     os.path.join(ROOT, "include", "kda.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -385,6 +385,114 @@ int fused_forward(const Shape& s, const KdaArgs* a, uint8_t* ws, const Layout& L
 }  // namespace
 }  // namespace kda
 
+namespace kda {
+namespace {
+
+// ---- intra-card context parallelism (KdaArgs.cp_chunks): the segmented view
+// of a fixed-length batch runs as a packed batch of B * nps sequences through
+// the public entry point, three times (kda_cp.cu has the scan and the reason).
+
+int cp_check(const KdaArgs* a, const Shape& s) {
+  if (a->cp_chunks < 0) return KDA_ERR_INVALID;
+  if (a->cu_seqlens || a->K != a->V || a->path == KDA_PATH_TWO_PASS || a->intra_tf32 || a->chunk_indices ||
+      a->chunk_offsets)
+    return KDA_ERR_UNSUPPORTED;
+  (void)s;
+  return KDA_OK;
+}
+
+// segments per sequence (1: nothing to split)
+int cp_segments(const KdaArgs* a, const Shape& s) { return (s.NT + a->cp_chunks - 1) / a->cp_chunks; }
+
+KdaArgs cp_sub_args(const KdaArgs* a, int nps, const int32_t* seg_cu) {
+  KdaArgs x = *a;
+  x.cu_seqlens = seg_cu;
+  x.N = a->B * nps;
+  x.T = a->B * a->T;
+  x.B = 1;
+  x.path = KDA_PATH_FUSED;
+  x.cp_chunks = 0;
+  x.profile_events = nullptr;
+  return x;
+}
+
+struct CpLayout {
+  size_t sub = 0, seg = 0, hs = 0, A = 0, Bs = 0, vz = 0, oz = 0, total = 0;
+  int nps = 1;
+};
+
+CpLayout cp_layout(const KdaArgs* a, const Shape& s) {
+  CpLayout c;
+  c.nps = cp_segments(a, s);
+  // any aligned non-null address stands for the segment table here: the
+  // size query dereferences no pointer
+  const KdaArgs sub = cp_sub_args(a, c.nps, reinterpret_cast<const int32_t*>(uintptr_t(1) << 20));
+  c.sub = align_up(kda_workspace_size(&sub));
+  size_t p = c.sub;
+  auto take = [&p](size_t bytes) {
+    const size_t at = p;
+    p = align_up(p + bytes);
+    return at;
+  };
+  const size_t nseg = size_t(s.B) * c.nps;
+  const size_t smat = nseg * s.Hv * s.K * s.V * 4;
+  c.seg = take((nseg + 1) * 4);
+  c.hs = take(smat);  // identity start states, then the scanned start states
+  c.A = take(smat);   // segment transitions
+  c.Bs = take(smat);  // segment end states from zero, then the last pass's (unused) end states
+  c.vz = take(size_t(s.BT) * s.Hv * s.V * 2);  // v = 0 for the transition pass
+  c.oz = take(size_t(s.BT) * s.Hv * s.V * 2);  // o of the first two passes (discarded)
+  c.total = p;
+  return c;
+}
+
+int cp_forward(const KdaArgs* a, const Shape& s, uint8_t* ws, size_t ws_bytes, cudaStream_t st) {
+  const CpLayout c = cp_layout(a, s);
+  if (ws_bytes < c.total) return KDA_ERR_WORKSPACE;
+  DeviceInfo d;
+  int rc = device_info(&d);
+  if (rc) return rc;
+  const int nseg = s.B * c.nps;
+  int32_t* seg = reinterpret_cast<int32_t*>(ws + c.seg);
+  float* hs = reinterpret_cast<float*>(ws + c.hs);
+  float* Am = reinterpret_cast<float*>(ws + c.A);
+  float* Bm = reinterpret_cast<float*>(ws + c.Bs);
+  kda_stream_t stream = reinterpret_cast<kda_stream_t>(st);
+  if (launch_cp_segments(seg, s.B, s.T, a->cp_chunks * kChunk, c.nps, st) != cudaSuccess) return KDA_ERR_LAUNCH;
+  // pass 1: each segment's end state from zero (o discarded)
+  KdaArgs p1 = cp_sub_args(a, c.nps, seg);
+  p1.initial_state = nullptr;
+  p1.o = ws + c.oz;
+  p1.final_state = Bm;
+  p1.Aqk = p1.Akk_inv = nullptr;
+  p1.W = p1.U = nullptr;
+  p1.G = nullptr;
+  p1.QG = nullptr;
+  rc = kda_chunk_fwd(&p1, ws, c.sub, stream);
+  if (rc) return rc;
+  // pass 2: each segment's transition, its end state from the identity with v = 0
+  if (launch_cp_identity(hs, (long long)nseg * s.Hv, s.K, st) != cudaSuccess) return KDA_ERR_LAUNCH;
+  if (cudaMemsetAsync(ws + c.vz, 0, size_t(s.BT) * s.Hv * s.V * 2, st) != cudaSuccess) return KDA_ERR_LAUNCH;
+  KdaArgs p2 = p1;
+  p2.v = ws + c.vz;
+  p2.initial_state = hs;
+  p2.final_state = Am;
+  rc = kda_chunk_fwd(&p2, ws, c.sub, stream);
+  if (rc) return rc;
+  // the scan: start states of the segments, final states of the sequences
+  if (launch_cp_scan(Am, Bm, a->initial_state, hs, a->final_state, s.B, c.nps, s.Hv, s.K, d.dev, st) !=
+      cudaSuccess)
+    return KDA_ERR_LAUNCH;
+  // pass 3: the outputs, from the scanned start states
+  KdaArgs p3 = cp_sub_args(a, c.nps, seg);
+  p3.initial_state = hs;
+  p3.final_state = Bm;
+  return kda_chunk_fwd(&p3, ws, c.sub, stream);
+}
+
+}  // namespace
+}  // namespace kda
+
 using namespace kda;
 
 extern "C" size_t kda_workspace_size(const KdaArgs* a) {
@@ -392,13 +500,39 @@ extern "C" size_t kda_workspace_size(const KdaArgs* a) {
   Mode mode;
   if (check_shape(a, &s) != KDA_OK || forward_mode(a, &mode) != KDA_OK) return 0;
   // the larger of the forward's and the intra primitive's needs
-  const size_t fwd = make_layout(s, a, mode).total, intra = make_layout(s, a, Mode::kIntra).total;
+  size_t fwd = make_layout(s, a, mode).total;
+  const size_t intra = make_layout(s, a, Mode::kIntra).total;
+  if (a->cp_chunks != 0) {
+    if (cp_check(a, s) != KDA_OK) return 0;
+    if (cp_segments(a, s) > 1) fwd = cp_layout(a, s).total;
+  }
   return fwd > intra ? fwd : intra;
 }
 
 extern "C" int kda_chunk_fwd(const KdaArgs* a, void* workspace, size_t ws_bytes, kda_stream_t stream) {
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (!a) return KDA_ERR_INVALID;
+  if (a->cp_chunks != 0) {
+    Shape s;
+    int rc = check_shape(a, &s);
+    if (rc) return rc;
+    rc = cp_check(a, s);
+    if (rc) return rc;
+    if (cp_segments(a, s) > 1 && s.BT > 0) {
+      if (!workspace) return KDA_ERR_INVALID;
+      // the profiling events bracket the whole call (all passes and the scan)
+      cudaEvent_t const* ev = reinterpret_cast<cudaEvent_t const*>(a->profile_events);
+      if (ev && cudaEventRecord(ev[0], st) != cudaSuccess) return KDA_ERR_LAUNCH;
+      rc = cp_forward(a, s, static_cast<uint8_t*>(workspace), ws_bytes, st);
+      if (rc == KDA_OK && ev &&
+          (cudaEventRecord(ev[1], st) != cudaSuccess || cudaEventRecord(ev[2], st) != cudaSuccess))
+        return KDA_ERR_LAUNCH;
+      return rc;
+    }
+    KdaArgs one = *a;  // a single segment: the plain forward
+    one.cp_chunks = 0;
+    return kda_chunk_fwd(&one, workspace, ws_bytes, stream);
+  }
   Mode mode;
   int rc = forward_mode(a, &mode);
   if (rc) return rc;

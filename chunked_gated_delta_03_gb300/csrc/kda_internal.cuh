@@ -200,5 +200,9 @@ cudaError_t launch_state(const Problem& P, const StateMaps& maps, const float* g
                          void* o, float* hT, int dev, cudaStream_t s);
 cudaError_t launch_fused(const Problem& P, const FusedArgs& A, const FusedMaps& maps, int dev, cudaStream_t s);
 cudaError_t launch_exact(const Problem& P, const ExactArgs& A, int dev, cudaStream_t s);
+cudaError_t launch_cp_segments(int32_t* seg_cu, int B, int T, int seg_tokens, int nps, cudaStream_t s);
+cudaError_t launch_cp_identity(float* h, long long nmat, int K, cudaStream_t s);
+cudaError_t launch_cp_scan(const float* A, const float* Bv, const float* h0, float* S_start, float* hT, int B,
+                           int nps, int Hv, int K, int dev, cudaStream_t s);
 
 }  // namespace kda

@@ -84,7 +84,7 @@ def _contig(*ts):
 
 def chunk_kda_fwd(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=None,
                   output_final_state=True, return_intermediates=False, return_G=False, return_QG=False,
-                  tf32=False, path="auto", chunk_table=None):
+                  tf32=False, path="auto", chunk_table=None, cp_chunks=0):
     """Chunked KDA forward.  Returns (o, final_state, intermediates).
 
     ``intermediates`` is None unless ``return_intermediates`` (then a dict with
@@ -97,13 +97,17 @@ def chunk_kda_fwd(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=N
     kernel, each (sequence, head) chain on one SM) or "two_pass" (intra-chunk
     kernel, then the state/output kernel).  ``chunk_table`` = (indices,
     offsets) from ``prepare_chunk_indices`` reuses a varlen chunk table instead
-    of building it again on the device.
+    of building it again on the device.  ``cp_chunks`` = n > 0 cuts every
+    sequence into segments of n chunks that run as chains of their own (intra-card
+    context parallelism: three passes and a scan over the segments; fixed-length
+    input with K == V only), for batches with far fewer chains than SMs.
     """
     if path not in _PATHS:
         raise ValueError(f"path must be one of {sorted(_PATHS)}")
     q, k, v, g, beta, cu_seqlens, initial_state = _contig(q, k, v, g, beta, cu_seqlens, initial_state)
     a, (B, T, Hq, Hv, K, V, N) = make_args(q, k, v, g, beta, scale, initial_state, cu_seqlens)
     a.path = _PATHS[path]
+    a.cp_chunks = int(cp_chunks)
     dev = q.device
     if chunk_table is not None:
         idx, off = (t.contiguous() for t in chunk_table)

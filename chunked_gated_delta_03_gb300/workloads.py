@@ -64,6 +64,10 @@ WORKLOADS = {
     "varlen_16k": Workload("varlen_16k", B=1, T=16384, Hq=64, Hv=64, K=128, V=128,
                            beta_dtype="bf16", initial_state=True,
                            varlen_total=16384, seed=4),
+    # few long chains (8 on a 152-SM GPU): the case intra-card context
+    # parallelism is for (cuLA PR #135, intra-card CP)
+    "long_16k_h8": Workload("long_16k_h8", B=1, T=16384, Hq=8, Hv=8, K=128, V=128,
+                            beta_dtype="bf16", initial_state=True, seed=5),
 }
 
 

@@ -165,6 +165,20 @@ typedef struct KdaArgs {
    * written.  Only one of the two set is KDA_ERR_INVALID. */
   const int32_t* chunk_indices;
   const int32_t* chunk_offsets;
+  /* Intra-card context parallelism (kda_chunk_fwd; cuLA PR #135, file list:
+   * cula/ops/kda/sm100/cp/pre_scan.py).  0: off.  n > 0: every sequence is cut
+   * into segments of n chunks that run as chains of their own: a first pass
+   * gives each segment's end state from zero, a second its K x K state
+   * transition (from the identity, with v = 0), a scan over the segments
+   * gives each one's start state and the sequence's final state, and a third
+   * pass from those start states writes the outputs.  Three passes over the
+   * data for n-fold more chains: it pays when N * Hv is far below the SM count
+   * and sequences are long (one 16k-token sequence with 8 heads).  Needs
+   * fixed-length input (cu_seqlens NULL), K == V, the fused path and no TF32
+   * option (else KDA_ERR_UNSUPPORTED); kda_workspace_size covers its buffers
+   * (three [B * segments, Hv, K, V] fp32 state arrays and two [B * T, Hv, V] bf16
+   * tiles).  The device status reports the last pass. */
+  int32_t cp_chunks;
 } KdaArgs;
 
 typedef KdaArgs KdaFwdArgs;

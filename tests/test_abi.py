@@ -161,3 +161,25 @@ def test_prepare_chunk_indices_rejects_bad_chunk(lib):
     for chunk in (0, -64):
         assert _lib.kda_prepare_chunk_indices(1 << 20, 1, 4, chunk, 1 << 20, 1 << 20, 1 << 20, 1 << 20, 0) \
             == _lib.KDA_ERR_INVALID
+
+
+def test_context_parallel_arguments(lib):
+    # intra-card context parallelism needs fixed-length input, K == V, the
+    # fused path and no TF32 option; its workspace adds the segment buffers
+    long = dict(T=64 * 40, Hq=2, Hv=2, K=64, V=64)
+    base = _lib.kda_workspace_size(_args(**long))
+    cp = _lib.kda_workspace_size(_args(cp_chunks=8, **long))
+    nseg, bt = 5, 64 * 40
+    assert cp >= base + 3 * nseg * 2 * 64 * 64 * 4 + 2 * bt * 2 * 64 * 2
+    # one segment covers the whole sequence: the plain forward and its workspace
+    assert _lib.kda_workspace_size(_args(cp_chunks=40, **long)) == base
+    for kw, code in ((dict(cp_chunks=-1), _lib.KDA_ERR_INVALID),
+                     (dict(cp_chunks=8, V=128), _lib.KDA_ERR_UNSUPPORTED),
+                     (dict(cp_chunks=8, path=_lib.KDA_PATH_TWO_PASS), _lib.KDA_ERR_UNSUPPORTED),
+                     (dict(cp_chunks=8, intra_tf32=1), _lib.KDA_ERR_UNSUPPORTED),
+                     (dict(cp_chunks=8, cu_seqlens=1 << 20, N=3), _lib.KDA_ERR_UNSUPPORTED)):
+        args = dict(long)
+        args.update(kw)
+        assert _lib.kda_chunk_fwd(_args(**args), 1 << 24, 1 << 30, 0) == code, kw
+        if code == _lib.KDA_ERR_UNSUPPORTED or kw.get("cp_chunks", 0) < 0:
+            assert _lib.kda_workspace_size(_args(**args)) == 0, kw

@@ -387,6 +387,47 @@ def test_intra_primitive_with_strong_gates():
     _check("QG", _np(intra["QG"]), want["QG"], **TOL_QG)
 
 
+def _ours_cp(inp, cp_chunks, inter=True):
+    return ops.chunk_kda_fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["scale"],
+                             inp["initial_state"], None, output_final_state=True, return_intermediates=inter,
+                             cp_chunks=cp_chunks)
+
+
+def test_context_parallel_long_sequence_matches_oracle():
+    # one 16k-token sequence with 8 heads (8 chains on the GPU): cut into
+    # segments of 16 chunks, the 128 segment chains run in parallel, their
+    # start states come from the scan over segment transitions
+    host = make_inputs(WORKLOADS["long_16k_h8"])
+    inp = _cuda(host)
+    out = _ours_cp(inp, 16)
+    heads = [0, 5]
+    want = _oracle(host, heads=heads)
+    _compare(host, out, want, heads=heads, inter=True)
+    # and against the unsplit chains: the same numbers up to bf16 rounding order
+    o0, fin0, _ = _ours(inp, inter=False)
+    _check("o vs unsplit", _np(out[0]), _np(o0), rel=3e-3)
+    _check("final vs unsplit", _np(out[1]), _np(fin0), rel=3e-3)
+
+
+def test_context_parallel_ragged_segments_match_oracle():
+    # segments of 4 chunks over 11-chunk sequences (the last segment partial,
+    # the last chunk a tail of 60 tokens), two sequences with initial states
+    host = make_inputs(WORKLOADS["tiny"], seed=47, B=2, T=700, Hq=2, Hv=2, K=64, V=64, initial_state=True,
+                       beta_dtype="bf16")
+    out = _ours_cp(_cuda(host), 4)
+    _compare(host, out, _oracle(host), inter=True)
+
+
+def test_context_parallel_single_segment_is_the_plain_call():
+    host = make_inputs(WORKLOADS["tiny"], seed=48, T=256, initial_state=True)
+    inp = _cuda(host)
+    o1, f1, i1 = _ours_cp(inp, 8)
+    o0, f0, i0 = _ours(inp, inter=True)
+    assert torch.equal(o1, o0) and torch.equal(f1, f0)
+    for key in i0:
+        assert torch.equal(i1[key], i0[key]), key
+
+
 @pytest.mark.parametrize("path", PATHS)
 def test_zero_beta_is_pure_gated_decay(path):
     # beta = 0: no delta updates.  Akk = 0, so Akk_inv is the identity and W, U

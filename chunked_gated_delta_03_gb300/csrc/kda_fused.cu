@@ -5,38 +5,44 @@
 // matrices, FP32 inverse of (I + Akk), W/U recompute) overlap the state and
 // output steps of chunk c (cuLA REPO_LAYOUT.md: chunk_delta_h.py, fwd_o.py).
 //
-// Warp roles (16 warps, 128 registers a thread):
-//   w0-w7    prep (thread = channel pair x 16-row quarter): loads of q, k, g,
-//            inclusive cumsum G, the gated operands Qg = q e^G, Kg = k e^G,
-//            Kd = k e^-G split into bf16 hi + lo, gamma = e^{G_last}.  Thread 0
-//            issues MMA1: D1 = [Qg; Kg] Kd^T with the hi/lo split (hi*hi +
-//            lo*hi, then hi*lo once Kd's low half has replaced the A operand's
-//            low half in the lo area).
-//   w8-w11   intra epilogue: Aqk rows (scale, causal mask) from D1 to the
-//            fp32 export and to a bf16 operand tile; Akk rows (beta, strict
-//            mask) to shared memory; the FP32 inverse X = (I + Akk)^-1 by
-//            16 x 16 blocks (diagonal blocks by forward substitution, the
-//            off-diagonal products as warp-level TF32 hi/lo MMAs), writing
-//            B2 = X diag(beta) as a bf16 tile as it goes; the Akk_inv export.  w8 lane 0 issues MMA2
-//            (W^T = Kg^T B2^T, U^T = v^T B2^T), the TMA copy of each chunk's v
-//            into its operand tile and the L2 prefetch of the next chunk's
-//            q, k, v, g; a tail chunk's v rows past its end are cleared.
-//   w12-w15  state (thread = value channel v): S^T lives in TMEM in fp32 and
-//            as a bf16 copy in shared memory (the A operand).  Per chunk, the
-//            threads copy W^T from TMEM into the W operand tile (and export W
-//            and U, thread = channel), w12 lane 0
-//            issues P^T = S^T W^T and O^T = S^T Qg^T, the threads form
-//            Delta^T = U^T - P^T (rows past the chunk's end zero), w12 lane 0
-//            issues S^T += Delta^T Kd and O^T += Delta^T Aqk^T, and the
-//            threads scale the state by gamma:
+// Warp roles (16 warps; setmaxnreg gives the prep 144 registers a thread, the
+// other two warpgroups 112):
+//   w0-w7    prep (thread = channel pair x 16-row quarter): loads of q, k, g
+//            (lanes 0 of w0-w2 prefetch the next chunk's into L2), inclusive
+//            cumsum G, the gated operands Qg = q e^G, Kg = k e^G, Kd = k e^-G
+//            as bf16 hi + lo pairs in registers, gamma = e^{G_last}; then the
+//            hi halves into the chunk's hi buffer and the lo halves into the
+//            lo area.  Thread 0 issues MMA1: D1 = [Qg; Kg] Kd^T with the hi/lo
+//            split (hi*hi + lo*hi, then hi*lo once Kd's low half has replaced
+//            the A operand's low half in the lo area).  A chunk past the gate
+//            range marks its chain for the exact path.
+//   w8-w11   intra epilogue (thread = row of D1): the whole row into
+//            registers, which frees D1 for the next MMA1; Aqk rows (causal
+//            mask) to the fp32 export and to a bf16 operand tile; Akk rows
+//            (beta, strict mask) to an fp32 scratch; the inverse
+//            X = (I + Akk)^-1 by 16 x 16 blocks (diagonal blocks by
+//            right-looking forward substitution, the off-diagonal products as
+//            warp-level TF32 hi/lo MMAs), writing B2 = X diag(beta) as a bf16
+//            tile as it goes.  w8 lane 0 issues MMA2 (W^T = Kg^T B2^T,
+//            U^T = v^T B2^T); a tail chunk's v rows past its end are cleared
+//            first; then the Akk_inv export by whole rows.
+//   w12-w15  state (thread = value channel v = TMEM lane): S^T lives in TMEM
+//            in fp32 and as a bf16 copy (the A operand of its MMAs).  Per
+//            chunk: W^T from TMEM into a token-major W tile in the chunk's
+//            dead Kg rows; w12 lane 0 issues P^T = S^T W^T and O^T = S^T Qg^T,
+//            the next chunk's v copy and W's TMA store; the threads form
+//            Delta^T = U^T - P^T into TMEM (rows past the chunk's end zero)
+//            and stage U token-major; w12 lane 0 issues S^T += Delta^T Kd and
+//            O^T += Delta^T Aqk^T and U's TMA store; the threads scale the
+//            state by gamma
 //              S <- Diag(e^{G_last}) (S + Kd^T Delta)
 //                 = Diag(e^{G_last}) S + (K e^{G_last - G})^T Delta,
-//            o = scale (Qg S + (Aqk / scale) Delta).
+//            hand the hi buffer back, and stage o = scale (Qg S + (Aqk / scale)
+//            Delta) token-major for its TMA store.
 //
 // The bf16 hi tiles of Qg, Kg and Kd are the operands of MMA1, of MMA2 (Kg as
 // an MN-major A) and of the state MMAs (Qg, Kd), so they are written once and
-// double-buffered by chunk parity.  The lo tiles live only until MMA1 ends;
-// their area then holds the inverse's fp32 scratch.  Every wait is bounded.
+// double-buffered by chunk parity.  Every wait is bounded.
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -656,7 +662,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       }
       __syncwarp();
       // ---- Akk_inv = X (lower triangle), by whole rows from the scratch (8
-      // passes of 8 rows x 16 column quads), while MMA2 runs
+      // passes of 8 rows x 16 column quads), while MMA2 runs; streaming stores
       if (A.Akk_inv) {
 #pragma unroll 2
         for (int it = 0; it < 8; ++it) {
@@ -664,7 +670,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
           const float4 xv = *reinterpret_cast<const float4*>(Xm + row * kLd + c4);
           const float4 o4 = make_float4(c4 <= row ? xv.x : 0.f, c4 + 1 <= row ? xv.y : 0.f,
                                         c4 + 2 <= row ? xv.z : 0.f, c4 + 3 <= row ? xv.w : 0.f);
-          if (row < L) *reinterpret_cast<float4*>(A.Akk_inv + (size_t(t0 + row) * P.Hv + hv) * 64 + c4) = o4;
+          if (row < L) __stcs(reinterpret_cast<float4*>(A.Akk_inv + (size_t(t0 + row) * P.Hv + hv) * 64 + c4), o4);
         }
       }
     }

@@ -122,9 +122,10 @@ __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bu
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // 32-byte global store of eight floats (the address must be 32-byte aligned):
-// one full sector per thread.
+// one full sector per thread, with the streaming cache hint (written once,
+// not read again by the kernel).
 __device__ __forceinline__ void st_global_v8(float* p, float4 a, float4 b) {
-  asm volatile("st.global.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "f"(a.x), "f"(a.y), "f"(a.z),
+  asm volatile("st.global.cs.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "f"(a.x), "f"(a.y), "f"(a.z),
                "f"(a.w), "f"(b.x), "f"(b.y), "f"(b.z), "f"(b.w)
                : "memory");
 }

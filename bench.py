@@ -8,7 +8,12 @@ inputs resident in HBM; the inputs (1.34 GB) are larger than L2 (129 MB), so
 no flush is needed between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--path auto|fused|two_pass] [--cp-chunks N]
   python bench.py --impl reference ...   # the FP64 CPU oracle, timed on the host
+
+A step's work ends with the exact path's check of the per-chain flags (no
+chunk of these workloads passes the gate range); `--cp-chunks N` times
+intra-card context parallelism (segments of N chunks; fixed-length, K == V).
 
 Multi-GPU (torchrun, one process per GPU): each rank runs an independent
 replica of the workload (the path has no exchange step); `value` is the

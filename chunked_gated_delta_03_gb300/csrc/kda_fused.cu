@@ -23,12 +23,12 @@
 //            X = (I + Akk)^-1 by 16 x 16 blocks (diagonal blocks by
 //            right-looking forward substitution, the off-diagonal products as
 //            warp-level TF32 hi/lo MMAs), writing B2 = X diag(beta) as a bf16
-//            tile as it goes.  w8 lane 0 issues MMA2 (W^T = Kg^T B2^T,
-//            U^T = v^T B2^T); a tail chunk's v rows past its end are cleared
-//            first; then the Akk_inv export by whole rows.
+//            tile as it goes; a tail chunk's v rows past its end are cleared;
+//            then B2 is handed to MMA2 and Akk_inv leaves by whole rows.
 //   w12-w15  state (thread = value channel v = TMEM lane): S^T lives in TMEM
 //            in fp32 and as a bf16 copy (the A operand of its MMAs).  Per
-//            chunk: W^T from TMEM into a token-major W tile in the chunk's
+//            chunk: w12 lane 0 issues MMA2 (W^T = Kg^T B2^T, U^T = v^T B2^T)
+//            once B2 is ready; W^T from TMEM into a token-major W tile in the chunk's
 //            dead Kg rows; w12 lane 0 issues P^T = S^T W^T and O^T = S^T Qg^T,
 //            the next chunk's v copy and W's TMA store; the threads form
 //            Delta^T = U^T - P^T into TMEM (rows past the chunk's end zero)
@@ -99,11 +99,11 @@ enum {
   bD1Empty = 2,  // intra epilogue read D1 -> MMA1                               (128)
   bHiFree = 4,   // [2] state done with hi buffer b (and its gamma, Aqk tile)    (128)
   bVFull = 6,    // TMA: v chunk landed                                          (1 + bytes)
-  bD2Full = 7,   // MMA2 done (after Aqk_b was written) -> intra epilogue, state (commit)
-  bD2Empty = 8,  // state read W^T / U^T / P^T -> MMA2                           (128)
+  bD2Full = 7,   // MMA2 done -> intra epilogue (B2 free), state                (commit)
+  bB2Ready = 8,  // intra wrote B2, the v tail, the Aqk tile -> MMA2 (state)    (128)
   bPDone = 10,   // P^T = S^T W^T done -> state                                  (commit)
   bHODone = 11,  // S^T += Delta^T Kd and O^T (both parts) done                  (commit)
-  bDrain = 12,   // [3] final drains of the three MMA issuers                    (commit)
+  bDrain = 12,   // [2] final drains of the two MMA issuers (prep, state)        (commit)
 };
 
 __device__ __forceinline__ uint32_t par(int n) { return uint32_t(n) & 1u; }
@@ -299,10 +299,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     mbar_init(&bar[bHiFree + 1], 128);
     mbar_init(&bar[bVFull], 1);
     mbar_init(&bar[bD2Full], 1);
-    mbar_init(&bar[bD2Empty], 128);
+    mbar_init(&bar[bB2Ready], 128);
     mbar_init(&bar[bPDone], 1);
     mbar_init(&bar[bHODone], 1);
-    for (int i = 0; i < 3; ++i) mbar_init(&bar[bDrain + i], 1);
+    for (int i = 0; i < 2; ++i) mbar_init(&bar[bDrain + i], 1);
     fence_mbar_init();
   }
   if (warp == kWarpIntra0) {
@@ -585,6 +585,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
           for (int rr = i + 1; rr < 16; ++rr) xc[rr] = fmaf(-ab[rr * kLd + i], xc[i], xc[rr]);
         uint8_t* b2 = sm + Lay::B2;
         const float bc = sB[base + cc];
+        // MMA2 of the last chunk has read B2 (its completion is D2 full); the
+        // barrier after this phase orders the R1 / R2 writers after it too
+        if (c >= 1) wait_bar(&bar[bD2Full], par(c - 1), abort_flag, P.status);
 #pragma unroll
         for (int rr = 0; rr < 16; ++rr) {
           Xm[(base + rr) * kLd + base + cc] = xc[rr];
@@ -642,25 +645,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
             *reinterpret_cast<uint4*>(vt + a * 8192 + (L + (i >> 3)) * 128 + (i & 7) * 16) = make_uint4(0, 0, 0, 0);
       }
       fence_proxy_async_smem();
-      named_bar_sync(kNbIntra, 128);
-      if (leader) {
-        // MMA2: W^T = Kg^T B2^T, U^T = v^T B2^T (M = 128 channels, N = 64, K = 64
-        // tokens).  Kg is read in place from the Kg rows of A1_hi as an MN-major
-        // operand (the next 64 channels one A1 atom, 16 KB, further on); v from
-        // its TMA tile (64-channel blocks 8 KB apart).  A K step of 16 tokens is
-        // 2048 B on the A side, 32 B on B2.
-        if (c >= 1) wait_bar(&bar[bD2Empty], par(c - 1), abort_flag, P.status);
-        tc_fence_after();
-        constexpr uint32_t idmn = idesc_bf16_f32(128, 64) | kIdescAMajorMN;
-        const uint32_t hi_addr = smem_u32(sm + Lay::HI + (c & 1) * Lay::kHi);
-        const uint64_t a_kg = sdesc_mnmajor_sw128(hi_addr + 8192, 16384);
-        const uint64_t a_v = sdesc_mnmajor_sw128(smem_u32(sm + Lay::VT), 8192);
-        const uint64_t b2 = sdesc_kmajor_sw128(smem_u32(sm + Lay::B2));
-        umma_k4(tmem + kColW, a_kg, b2, idmn, 0, 2048 / 16, 2);
-        umma_k4(tmem + kColU, a_v, b2, idmn, 0, 2048 / 16, 2);
-        umma_commit(&bar[bD2Full]);
-      }
-      __syncwarp();
+      mbar_arrive(&bar[bB2Ready]);  // B2, the v tail and the Aqk tile are ready: MMA2 may start
+      named_bar_sync(kNbIntra, 128);  // every warp's X blocks are in the scratch
+
       // ---- Akk_inv = X (lower triangle), by whole rows from the scratch (8
       // passes of 8 rows x 16 column quads), while MMA2 runs; streaming stores
       if (A.Akk_inv) {
@@ -673,11 +660,6 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
           if (row < L) __stcs(reinterpret_cast<float4*>(A.Akk_inv + (size_t(t0 + row) * P.Hv + hv) * 64 + c4), o4);
         }
       }
-    }
-    if (leader) {
-      // after an abort: the last MMA2 must land before exit
-      umma_commit(&bar[bDrain + 1]);
-      mbar_wait(&bar[bDrain + 1], 0, kDrainNs);
     }
 
   } else {
@@ -739,8 +721,27 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       const uint32_t hi_addr = smem_u32(hi);
       // ---- W^T (TMEM lane = channel k) into the W tile, token-major, in the
       // Kg rows of this chunk's A1_hi (MMA2 was their last reader): atom a at
-      // hi + 16 KB a + 8 KB.  MMA2 commits after the Aqk_b tile of chunk c was
-      // written, so D2 full also covers that tile.
+      // hi + 16 KB a + 8 KB.  The intra warps signalled B2 ready after the
+      // Aqk_b tile of chunk c was written, so D2 full also covers that tile.
+      if (leader) {
+        // MMA2: W^T = Kg^T B2^T, U^T = v^T B2^T (M = 128 channels, N = 64, K = 64
+        // tokens), once the intra warps have written B2 (and cleared the v
+        // tail); this pass is done with last chunk's W^T / U^T / P^T.  Kg is
+        // read in place from the Kg rows of A1_hi as an MN-major operand (the
+        // next 64 channels one A1 atom, 16 KB, further on); v from its TMA tile
+        // (64-channel blocks 8 KB apart).  A K step of 16 tokens is 2048 B on the
+        // A side, 32 B on B2.
+        wait_bar(&bar[bB2Ready], par(c), abort_flag, P.status);
+        tc_fence_after();
+        constexpr uint32_t idmn = idesc_bf16_f32(128, 64) | kIdescAMajorMN;
+        const uint64_t a_kg = sdesc_mnmajor_sw128(hi_addr + 8192, 16384);
+        const uint64_t a_v = sdesc_mnmajor_sw128(smem_u32(sm + Lay::VT), 8192);
+        const uint64_t b2 = sdesc_kmajor_sw128(smem_u32(sm + Lay::B2));
+        umma_k4(tmem + kColW, a_kg, b2, idmn, 0, 2048 / 16, 2);
+        umma_k4(tmem + kColU, a_v, b2, idmn, 0, 2048 / 16, 2);
+        umma_commit(&bar[bD2Full]);
+      }
+      __syncwarp();
       wait_bar(&bar[bD2Full], par(c), abort_flag, P.status);
       tc_fence_after();
       if (leader && c + 1 < nch) {
@@ -819,7 +820,6 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&bar[bD2Empty]);
       named_bar_sync(kNbState, 128);
       if (leader) {
         // S^T += Delta^T Kd (Kd token rows of B1_hi as an MN-major B: 64-channel
@@ -901,8 +901,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       // after an abort: the last v copy (issued here or by the intra leader) lands before exit
       mbar_wait(&bar[bVFull], par(nch - 1), kDrainNs);
       bulk_wait_all();
-      umma_commit(&bar[bDrain + 2]);
-      mbar_wait(&bar[bDrain + 2], 0, kDrainNs);
+      umma_commit(&bar[bDrain + 1]);
+      mbar_wait(&bar[bDrain + 1], 0, kDrainNs);
     }
   }
   tc_fence_before();

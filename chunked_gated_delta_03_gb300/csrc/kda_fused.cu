@@ -15,10 +15,13 @@
 //            lo area.  Thread 0 issues MMA1: D1 = [Qg; Kg] Kd^T with the hi/lo
 //            split (hi*hi + lo*hi, then hi*lo once Kd's low half has replaced
 //            the A operand's low half in the lo area).  A chunk past the gate
-//            range marks its chain for the exact path.
+//            range marks its chain for the exact path.  While the next
+//            chunk's loads are in flight, w0, w1, w4 and w5 (whose TMEM lane
+//            quarters hold D1's Qg rows) write the last chunk's fp32 Aqk
+//            export (scale, causal mask) straight from D1.
 //   w8-w11   intra epilogue (thread = row of D1): the whole row into
 //            registers, which frees D1 for the next MMA1; Aqk rows (causal
-//            mask) to the fp32 export and to a bf16 operand tile; Akk rows
+//            mask) to a bf16 operand tile; Akk rows
 //            (beta, strict mask) to an fp32 scratch; the inverse
 //            X = (I + Akk)^-1 by 16 x 16 blocks (diagonal blocks by
 //            right-looking forward substitution, the off-diagonal products as
@@ -28,8 +31,8 @@
 //   w12-w15  state (thread = value channel v = TMEM lane): S^T lives in TMEM
 //            in fp32 and as a bf16 copy (the A operand of its MMAs).  Per
 //            chunk: w12 lane 0 issues MMA2 (W^T = Kg^T B2^T, U^T = v^T B2^T)
-//            once B2 is ready; W^T from TMEM into a token-major W tile in the chunk's
-//            dead Kg rows; w12 lane 0 issues P^T = S^T W^T and O^T = S^T Qg^T,
+//            once B2 is ready; W^T from TMEM into a token-major W tile in the
+//            chunk's dead Kg rows; w12 lane 0 issues P^T = S^T W^T and O^T = S^T Qg^T,
 //            the next chunk's v copy and W's TMA store; the threads form
 //            Delta^T = U^T - P^T into TMEM (rows past the chunk's end zero)
 //            and stage U token-major; w12 lane 0 issues S^T += Delta^T Kd and
@@ -332,6 +335,35 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     float* part_base = reinterpret_cast<float*>(sm + Lay::PART);
     float* gam_base = reinterpret_cast<float*>(sm + Lay::GAM);
     uint8_t* lo = sm + Lay::LO;
+    // The fp32 Aqk export (scaled, causal mask) of chunk cc from D1's Qg rows
+    // (TMEM lanes 0-63), by the prep warps whose lane quarter holds them:
+    // warps 0, 1 columns 0-31, warps 4, 5 columns 32-63, thread = row
+    const bool aqk_w = A.Aqk != nullptr && (warp & 2) == 0;
+    auto export_aqk = [&](int cc) {
+      const int tc = bos + cc * kChunk, Lc = min(kChunk, len - cc * kChunk);
+      const int r = 32 * (warp & 1) + lane, cb = 32 * (warp >> 2);
+      wait_bar(&bar[bD1Full], par(cc), abort_flag, P.status);
+      tc_fence_after();
+      float* arow = A.Aqk + (size_t(tc + r) * P.Hv + hv) * 64;
+      // 8 columns at a time: the next chunk's loads hold 64 registers meanwhile
+#pragma unroll 1
+      for (int h = cb; h < cb + 32; h += 8) {
+        uint32_t x[8];
+        tmem_ld_x8(tmem_addr(tmem, 32 * (warp & 1), kColD1 + h), x);  // warp-collective
+        if (r < Lc) {
+          float f[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) f[j] = (h + j <= r) ? P.scale * __uint_as_float(x[j]) : 0.f;
+          const float4 lo4 = make_float4(f[0], f[1], f[2], f[3]), hi4 = make_float4(f[4], f[5], f[6], f[7]);
+          if (A.aqk_v8) {
+            st_global_v8(arow + h, lo4, hi4);  // a whole 32-byte sector per thread
+          } else {
+            __stcs(reinterpret_cast<float4*>(arow + h), lo4);
+            __stcs(reinterpret_cast<float4*>(arow + h + 4), hi4);
+          }
+        }
+      }
+    };
     for (int c = 0; c < nch; ++c) {
       const int t0 = bos + c * kChunk, L = min(kChunk, len - c * kChunk);
       // ---- L2 prefetch of the next chunk's q, k and g (a box of 64 token rows
@@ -358,6 +390,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
           k2[rr] = __ldg(reinterpret_cast<const uint32_t*>(reinterpret_cast<const __nv_bfloat16*>(A.k) + tq * K + c0));
         }
       }
+      // ---- last chunk's Aqk export while the loads are in flight (D1 holds
+      // it until this iteration's MMA1)
+      if (aqk_w && c >= 1) export_aqk(c - 1);
       // ---- cumsum offsets across the row quarters
       float* part = part_base + (c & 1) * 4 * K;
       if (kact) {
@@ -439,6 +474,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         }
       }
       fence_proxy_async_smem();
+      tc_fence_before();  // the Aqk export's D1 reads come before MMA1 overwrites D1
       named_bar_sync(kNbPrep, kPrepThreadsF);
       // ---- MMA1 (thread 0): hi*hi + lo*hi; atoms of 64 channels, A 128 rows
       // (1024 descriptor units apart), B 64 rows (512)
@@ -473,6 +509,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       }
       __syncwarp();
     }
+    if (aqk_w && nch >= 1) export_aqk(nch - 1);
     if (mma_leader) {
       umma_commit(&bar[bDrain]);
       mbar_wait(&bar[bDrain], 0, kDrainNs);
@@ -549,24 +586,6 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
           *reinterpret_cast<uint4*>(aqkb + sw128_offset(uint32_t(r), uint32_t(i), 64)) = pack8(f);
         }
         fence_proxy_async_smem();
-        // and the fp32 Aqk row (scaled, causal mask), 32 bytes a store when
-        // the output is 32-byte aligned
-        if (A.Aqk && r < L) {
-          float* arow = A.Aqk + (size_t(t0 + r) * P.Hv + hv) * 64;
-#pragma unroll
-          for (int i = 0; i < 64; i += 8) {
-            float f[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) f[j] = (i + j <= r) ? P.scale * __uint_as_float(x[i + j]) : 0.f;
-            const float4 lo4 = make_float4(f[0], f[1], f[2], f[3]), hi4 = make_float4(f[4], f[5], f[6], f[7]);
-            if (A.aqk_v8) {
-              st_global_v8(arow + i, lo4, hi4);  // a whole 32-byte sector per thread
-            } else {
-              *reinterpret_cast<float4*>(arow + i) = lo4;
-              *reinterpret_cast<float4*>(arow + i + 4) = hi4;
-            }
-          }
-        }
       }
       named_bar_sync(kNbIntra, 128);
       if (akk) {

@@ -281,6 +281,42 @@ def test_caller_chunk_table_gives_the_same_results(path):
 
 
 @pytest.mark.parametrize("path", PATHS)
+def test_aqk_16_bytes_off_a_32_byte_boundary_gives_the_same_results(path):
+    # Aqk rows leave in 32-byte stores when the buffer is 32-byte aligned and
+    # in 16-byte stores otherwise (the API asks for 16); Akk_inv moves by the
+    # same offset.  Only the store width differs, so the values are the same
+    # bits as from aligned buffers, on a chain with a partial tail chunk.
+    inp = _cuda(make_inputs(WORKLOADS["tiny"], seed=81, T=200, initial_state=True))
+    stream = torch.cuda.current_stream().cuda_stream
+    outs = []
+    for shift in (0, 4):                         # fp32 elements: 0 or 16 bytes past a 256-byte base
+        a, (B, T, Hq, Hv, K, V, N) = ops.make_args(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+                                                   inp["scale"], inp["initial_state"], inp["cu_seqlens"])
+        a.path = ops._PATHS[path]
+        bufs = {"o": torch.empty(B, T, Hv, V, dtype=torch.bfloat16, device="cuda"),
+                "final_state": torch.empty(N, Hv, K, V, dtype=torch.float32, device="cuda"),
+                "W": torch.empty(B, T, Hv, K, dtype=torch.bfloat16, device="cuda"),
+                "U": torch.empty(B, T, Hv, V, dtype=torch.bfloat16, device="cuda")}
+        for name in ("Aqk", "Akk_inv"):
+            n = B * T * Hv * 64
+            bufs[name] = torch.full((n + shift,), float("nan"), dtype=torch.float32,
+                                    device="cuda")[shift:].view(B, T, Hv, 64)
+        assert bufs["Aqk"].data_ptr() % 32 == (16 if shift else 0)
+        for name, t in bufs.items():
+            setattr(a, name, t.data_ptr())
+        n = _lib.kda_workspace_size(a)
+        ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+        assert _lib.kda_chunk_fwd(a, ws.data_ptr(), n, stream) == _lib.KDA_OK
+        assert ops.device_status(ws) == _lib.KDA_OK
+        outs.append(bufs)
+    for name in outs[0]:
+        assert torch.equal(outs[0][name], outs[1][name]), name
+    want = _oracle(inp)
+    _check("Aqk", _np(outs[1]["Aqk"]), want["Aqk"], **TOL_FP32)
+    _check("Akk_inv", _np(outs[1]["Akk_inv"]), want["Akk_inv"], **TOL_FP32)
+
+
+@pytest.mark.parametrize("path", PATHS)
 def test_bad_caller_chunk_table_sets_device_status(path):
     inp = _cuda(make_inputs(WORKLOADS["tiny"], seed=72, lengths=(100, 30, 156)))
     idx, off = ops.prepare_chunk_indices(inp["cu_seqlens"], 64)
